@@ -1,0 +1,176 @@
+/*
+ * zpp.h -- C ABI of the GB300 (sm_103a) ZeRO++ block-quantisation hot path.
+ *
+ * Pages cited (by title; the section follows the label):
+ *   [ZeRO++ summary]  "ZeRO++: Extremely Efficient Collective Communication for Large
+ *                      Model Training" (atlas.scime.ai summary)
+ *   [ZeRO++ abstract] "ZeRO++: Extremely Efficient Collective Communication for Giant
+ *                      Model Training" (mlsanity.com record, arXiv abstract)
+ *   [LIT-102]         "LIT-102: ZeRO++: Extremely Efficient Collective Communication
+ *                      for Giant Model Training" (anthology-of-the-sota record)
+ *
+ * What the calls compute (the pages fix the structure, not the formula; this is the
+ * reading every entry point implements, bit for bit):
+ *   per block of `block` consecutive elements (the last block may be shorter):
+ *     amax  = max |x|;  scale = fp32(amax / qmax);  inv = fp32(qmax / amax)
+ *     q     = clamp(rint_to_even(fp32(x * inv)), -qmax, qmax),  qmax = 2^(bits-1) - 1
+ *     amax == 0 or inv not finite  ->  scale = 0 and every q = 0
+ *   dequantise: y = fp32((float)q * scale), then round-to-nearest-even into y's type.
+ *   Every fp32 operation is rounded on its own (no FMA); sums start at +0.0f and add
+ *   sources in ascending order.
+ *
+ * Storage: INT8 codes are two's-complement bytes; INT4 codes are two's-complement
+ * nibbles, element 2i in the LOW nibble of byte i and 2i+1 in the high nibble (an odd
+ * trailing element leaves the high nibble 0). Scales are a separate fp32 array, one
+ * per block, in block order.
+ *
+ * Virtual topology (qgZ): N nodes x M GPUs per node, W = N*M ranks, rank r = n*M + l.
+ * Ranks are HBM buffers laid out back to back ([W][...]); the all-to-all exchanges are
+ * index maps over them, no data is moved between the steps.
+ *   E = elements per rank, S = E / W (the slice each rank owns), C = N*S (hop-1 chunk).
+ *
+ * Conventions for every entry point:
+ *   - All buffer pointers are DEVICE pointers owned by the caller. The library
+ *     allocates nothing, never synchronises, and only enqueues kernels on `stream`
+ *     (0 = the legacy default stream).
+ *   - Inputs and outputs must not overlap.
+ *   - Arguments are checked on the host before any launch; on an error nothing is
+ *     launched and nothing is written.
+ *   - Alignment: element and code buffers (x, y, grads, codes, out) must be 32-byte
+ *     aligned (the kernels move 256-bit vectors); scale arrays 4-byte aligned.
+ *   - n == 0 (or a zero-sized topology payload) returns ZPP_OK and launches nothing.
+ *   - A launch failure is reported as ZPP_ERR_CUDA (from cudaGetLastError); an
+ *     asynchronous fault surfaces at the caller's next synchronisation.
+ *   - Inputs must be finite; NaN or Inf inputs give unspecified codes.
+ */
+#ifndef ZPP_H
+#define ZPP_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define ZPP_API __attribute__((visibility("default")))
+#else
+#define ZPP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zpp_status {
+  ZPP_OK = 0,
+  ZPP_ERR_INVALID_ARG = 1, /* bad bits / block / size / topology / null pointer */
+  ZPP_ERR_MISALIGNED = 2,  /* a pointer breaks the alignment rule above */
+  ZPP_ERR_UNSUPPORTED = 3, /* a valid but unimplemented dtype combination */
+  ZPP_ERR_CUDA = 4         /* the CUDA runtime reported an error at launch */
+} zpp_status;
+
+typedef enum zpp_dtype { ZPP_F16 = 0, ZPP_BF16 = 1, ZPP_F32 = 2 } zpp_dtype;
+
+typedef struct zpp_topology {
+  int32_t num_nodes;     /* N >= 1 */
+  int32_t gpus_per_node; /* M >= 1 */
+} zpp_topology;
+
+/* Limits checked by every entry point. */
+#define ZPP_MIN_BLOCK 64
+#define ZPP_MAX_BLOCK 4096
+#define ZPP_MAX_ELEMS (((int64_t)1) << 38)
+
+/*
+ * qwZ step 1 -- block-wise symmetric quantisation of a weight shard before the forward
+ * all-gather ([ZeRO++ summary] Approach: block-wise INT8 weight quantisation;
+ * [ZeRO++ abstract]: block-quantisation based all-gather; [LIT-102] Key takeaways:
+ * block-wise rather than per-tensor). Also the INT4 gradient quantiser of qgZ.
+ *   x      : [n] elements of x_dt (ZPP_F16 or ZPP_BF16; ZPP_F32 -> ZPP_ERR_UNSUPPORTED)
+ *   n      : element count, 0 <= n <= ZPP_MAX_ELEMS
+ *   block  : power of two in [64, 4096]
+ *   bits   : 8 or 4
+ *   codes  : out, zpp_code_bytes(n, bits) bytes
+ *   scales : out, zpp_num_scales(n, block) floats
+ * Shards whose sizes are multiples of `block` can be quantised in one call over their
+ * concatenation: the result is identical to one call per shard.
+ */
+ZPP_API zpp_status zpp_quant_blockwise(const void* x, zpp_dtype x_dt, int64_t n, int32_t block,
+                               int32_t bits, void* codes, float* scales, cudaStream_t stream);
+
+/*
+ * qwZ step 2 -- dequantisation of the gathered codes after the all-gather
+ * ([ZeRO++ summary] Approach; [ZeRO++ abstract]: block-quantisation based all-gather).
+ *   codes  : [zpp_code_bytes(n, bits)] bytes; scales: [zpp_num_scales(n, block)] floats
+ *   y      : out, [n] elements of y_dt (ZPP_F16, ZPP_BF16 or ZPP_F32)
+ * Other arguments as in zpp_quant_blockwise.
+ */
+ZPP_API zpp_status zpp_dequant_blockwise(const void* codes, const float* scales, int64_t n,
+                                 int32_t block, int32_t bits, void* y, zpp_dtype y_dt,
+                                 cudaStream_t stream);
+
+/*
+ * qgZ step 1 -- tensor-slice reordering plus block quantisation of every rank's
+ * gradient before the 2-hop all-to-all ([ZeRO++ summary] Approach: slices reordered
+ * so each reduced slice lands on its owner; INT4 gradient reduction).
+ * Each rank's E elements are W slices of S; original slice j = n_d*M + l_d (owned by
+ * rank j) is written at position p = l_d*N + n_d, so the reordered buffer is M chunks
+ * of C = N*S, chunk l going to local peer l in hop 1. Quantisation then runs over the
+ * reordered buffer (blocks never straddle slices).
+ *   grads          : [W][E] elements of g_dt (ZPP_F16 or ZPP_BF16)
+ *   elems_per_rank : E, a multiple of W*block, E < 2^31
+ *   bits           : 4 (the pages' INT4); 8 is accepted as an extension
+ *   codes          : out, [W][zpp_code_bytes(E, bits)]
+ *   scales         : out, [W][E/block]
+ */
+ZPP_API zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
+                                 int32_t block, int32_t bits, zpp_topology topo,
+                                 void* codes, float* scales, cudaStream_t stream);
+
+/*
+ * qgZ step 2 -- the fused kernel of the intra-node hop: every receiver (n, l)
+ * dequantises chunk l of the M ranks of its node, sums them in fp32 (l' ascending) and
+ * requantises the sums by blocks for the inter-node hop ([ZeRO++ summary] Approach:
+ * dequantise before reduction; Measured effects table: fusion kernel; [LIT-102] Key
+ * takeaways: reduce locally in higher precision). K = M chunks are read once.
+ *   codes, scales  : the outputs of zpp_qgz_reorder_quant
+ *   out_codes      : out, [W][zpp_code_bytes(C, bits)]
+ *   out_scales     : out, [W][C/block]
+ */
+ZPP_API zpp_status zpp_dequant_reduce_requant(const void* codes, const float* scales,
+                                      int64_t elems_per_rank, int32_t block, int32_t bits,
+                                      zpp_topology topo, void* out_codes, float* out_scales,
+                                      cudaStream_t stream);
+
+/*
+ * qgZ step 3 -- the inter-node hop's final dequantise-reduce: receiver (n, l)
+ * dequantises slice n of the hop-1 output of rank (n', l) for n' = 0..N-1 and sums in
+ * fp32 (n' ascending). The result is the SUM over all W ranks of the receiver's own
+ * slice; scaling by 1/W for an average is left to the caller ([ZeRO++ summary]
+ * Approach; [ZeRO++ abstract]: quantised gradient averaging).
+ *   codes, scales  : the outputs of zpp_dequant_reduce_requant
+ *   out            : out, [W][S] fp32
+ */
+ZPP_API zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t elems_per_rank,
+                              int32_t block, int32_t bits, zpp_topology topo, float* out,
+                              cudaStream_t stream);
+
+/* Bytes of packed codes for n elements: n for INT8, ceil(n/2) for INT4; -1 on bad bits. */
+ZPP_API int64_t zpp_code_bytes(int64_t n, int32_t bits);
+
+/* Number of scales for n elements: ceil(n / block); -1 on a bad block. */
+ZPP_API int64_t zpp_num_scales(int64_t n, int32_t block);
+
+/* Static, never-NULL description of a status code. */
+ZPP_API const char* zpp_status_string(zpp_status status);
+
+/*
+ * Measurement helper (no counterpart in the pages): a 256-bit streaming device copy
+ * used as the same-run HBM reference next to the kernels above.
+ *   src, dst : 32-byte aligned device buffers; bytes: a multiple of 32.
+ */
+ZPP_API zpp_status zpp_device_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZPP_H */

@@ -1,0 +1,217 @@
+"""ctypes binding of ``libzpp.so`` (argument marshalling only).
+
+The raw functions carry the C names and take device addresses as integers; the tensor
+helpers below allocate outputs with torch on the input's device, pass pointers and the
+current CUDA stream, and raise on a non-OK status. Every step of the computation runs
+in the library's kernels: there is no CPU path, and a missing library or a CPU tensor
+is an error.
+"""
+import ctypes
+import os
+import re
+
+from . import build as _build
+
+ZPP_OK, ZPP_ERR_INVALID_ARG, ZPP_ERR_MISALIGNED, ZPP_ERR_UNSUPPORTED, ZPP_ERR_CUDA = range(5)
+ZPP_F16, ZPP_BF16, ZPP_F32 = 0, 1, 2
+
+HEADER = os.path.join(_build.ROOT, "include", "zpp.h")
+
+
+class Topology(ctypes.Structure):
+    _fields_ = [("num_nodes", ctypes.c_int32), ("gpus_per_node", ctypes.c_int32)]
+
+
+class ZppError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {zpp_status_string(status)}")
+
+
+_lib = None
+
+
+def lib_path():
+    return _build.LIB
+
+
+def lib():
+    """Load libzpp.so (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"{_build.LIB} is missing: build it with __graft_entry__.build() "
+                           "(there is no fallback path)")
+    L = ctypes.CDLL(_build.LIB)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    sig = {
+        "zpp_quant_blockwise": [vp, i32, i64, i32, i32, vp, vp, vp],
+        "zpp_dequant_blockwise": [vp, vp, i64, i32, i32, vp, i32, vp],
+        "zpp_qgz_reorder_quant": [vp, i32, i64, i32, i32, Topology, vp, vp, vp],
+        "zpp_dequant_reduce_requant": [vp, vp, i64, i32, i32, Topology, vp, vp, vp],
+        "zpp_dequant_reduce": [vp, vp, i64, i32, i32, Topology, vp, vp],
+        "zpp_device_copy": [vp, vp, i64, vp],
+    }
+    for name, args in sig.items():
+        f = getattr(L, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    L.zpp_code_bytes.argtypes = [i64, i32]
+    L.zpp_code_bytes.restype = i64
+    L.zpp_num_scales.argtypes = [i64, i32]
+    L.zpp_num_scales.restype = i64
+    L.zpp_status_string.argtypes = [ctypes.c_int]
+    L.zpp_status_string.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def declared_symbols(header=HEADER):
+    """Names of the functions the public header declares."""
+    text = open(header).read()
+    return sorted(set(re.findall(r"ZPP_API\s+[\w\s\*]*?\b(zpp_\w+)\s*\(", text)))
+
+
+# ----------------------------------------------------------------------------- raw ABI
+def zpp_quant_blockwise(x, x_dt, n, block, bits, codes, scales, stream=0):
+    return lib().zpp_quant_blockwise(x, x_dt, n, block, bits, codes, scales, stream)
+
+
+def zpp_dequant_blockwise(codes, scales, n, block, bits, y, y_dt, stream=0):
+    return lib().zpp_dequant_blockwise(codes, scales, n, block, bits, y, y_dt, stream)
+
+
+def zpp_qgz_reorder_quant(grads, g_dt, elems_per_rank, block, bits, topo, codes, scales, stream=0):
+    return lib().zpp_qgz_reorder_quant(grads, g_dt, elems_per_rank, block, bits, topo, codes,
+                                       scales, stream)
+
+
+def zpp_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits, topo, out_codes,
+                               out_scales, stream=0):
+    return lib().zpp_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits, topo,
+                                            out_codes, out_scales, stream)
+
+
+def zpp_dequant_reduce(codes, scales, elems_per_rank, block, bits, topo, out, stream=0):
+    return lib().zpp_dequant_reduce(codes, scales, elems_per_rank, block, bits, topo, out, stream)
+
+
+def zpp_device_copy(src, dst, nbytes, stream=0):
+    return lib().zpp_device_copy(src, dst, nbytes, stream)
+
+
+def zpp_code_bytes(n, bits):
+    return int(lib().zpp_code_bytes(n, bits))
+
+
+def zpp_num_scales(n, block):
+    return int(lib().zpp_num_scales(n, block))
+
+
+def zpp_status_string(status):
+    return lib().zpp_status_string(int(status)).decode()
+
+
+# ----------------------------------------------------------------------------- tensors
+def _torch():
+    import torch
+    return torch
+
+
+def _dt(t):
+    torch = _torch()
+    return {torch.float16: ZPP_F16, torch.bfloat16: ZPP_BF16, torch.float32: ZPP_F32}[t]
+
+
+def _cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("zpp operates on CUDA tensors only (no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("zpp needs contiguous tensors")
+
+
+def _stream(t):
+    return _torch().cuda.current_stream(t.device).cuda_stream
+
+
+def _check(status, where):
+    if status != ZPP_OK:
+        raise ZppError(status, where)
+
+
+def quant_blockwise(x, block, bits, codes=None, scales=None):
+    """x (fp16/bf16, any shape) -> (codes uint8[code_bytes], scales fp32[num_scales])."""
+    torch = _torch()
+    _cuda(x)
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(zpp_code_bytes(n, bits), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(zpp_num_scales(n, block), dtype=torch.float32, device=x.device)
+    _check(zpp_quant_blockwise(x.data_ptr(), _dt(x.dtype), n, block, bits, codes.data_ptr(),
+                               scales.data_ptr(), _stream(x)), "zpp_quant_blockwise")
+    return codes, scales
+
+
+def dequant_blockwise(codes, scales, n, block, bits, dtype=None, y=None):
+    """codes, scales -> y[n] of `dtype` (default fp16)."""
+    torch = _torch()
+    _cuda(codes, scales)
+    if y is None:
+        y = torch.empty(n, dtype=dtype or torch.float16, device=codes.device)
+    _check(zpp_dequant_blockwise(codes.data_ptr(), scales.data_ptr(), n, block, bits,
+                                 y.data_ptr(), _dt(y.dtype), _stream(codes)),
+           "zpp_dequant_blockwise")
+    return y
+
+
+def qgz_reorder_quant(grads, block, bits, N, M, codes=None, scales=None):
+    """grads [W][E] (fp16/bf16) -> (codes uint8 [W][code_bytes(E)], scales fp32 [W][E/block])."""
+    torch = _torch()
+    _cuda(grads)
+    W = N * M
+    E = grads.numel() // W
+    if codes is None:
+        codes = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=grads.device)
+    if scales is None:
+        scales = torch.empty((W, E // block), dtype=torch.float32, device=grads.device)
+    _check(zpp_qgz_reorder_quant(grads.data_ptr(), _dt(grads.dtype), E, block, bits,
+                                 Topology(N, M), codes.data_ptr(), scales.data_ptr(),
+                                 _stream(grads)), "zpp_qgz_reorder_quant")
+    return codes, scales
+
+
+def dequant_reduce_requant(codes, scales, E, block, bits, N, M, out_codes=None, out_scales=None):
+    """Intra-node hop -> (codes uint8 [W][code_bytes(E/M)], scales fp32 [W][E/M/block])."""
+    torch = _torch()
+    _cuda(codes, scales)
+    W, C = N * M, E // M
+    if out_codes is None:
+        out_codes = torch.empty((W, zpp_code_bytes(C, bits)), dtype=torch.uint8, device=codes.device)
+    if out_scales is None:
+        out_scales = torch.empty((W, C // block), dtype=torch.float32, device=codes.device)
+    _check(zpp_dequant_reduce_requant(codes.data_ptr(), scales.data_ptr(), E, block, bits,
+                                      Topology(N, M), out_codes.data_ptr(), out_scales.data_ptr(),
+                                      _stream(codes)), "zpp_dequant_reduce_requant")
+    return out_codes, out_scales
+
+
+def dequant_reduce(codes, scales, E, block, bits, N, M, out=None):
+    """Inter-node hop -> fp32 [W][E/W], each rank's summed owner slice."""
+    torch = _torch()
+    _cuda(codes, scales)
+    W = N * M
+    if out is None:
+        out = torch.empty((W, E // W), dtype=torch.float32, device=codes.device)
+    _check(zpp_dequant_reduce(codes.data_ptr(), scales.data_ptr(), E, block, bits, Topology(N, M),
+                              out.data_ptr(), _stream(codes)), "zpp_dequant_reduce")
+    return out
+
+
+def device_copy(src, dst):
+    _cuda(src, dst)
+    nbytes = src.numel() * src.element_size()
+    _check(zpp_device_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(src)), "zpp_device_copy")
+    return dst

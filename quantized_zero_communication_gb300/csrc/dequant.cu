@@ -1,0 +1,139 @@
+// dequant.cu -- K2: qwZ dequantisation after the all-gather, y = (float)q * scale rounded
+// into fp16, bf16 or fp32.
+//
+// Warp tile: 4 rows of 512 elements. Per row a lane reads 16 codes (16 bytes INT8, 8
+// bytes INT4) and one block scale (the 16 elements never straddle a block, block >= 64)
+// and writes 16 outputs with 256-bit stores (one for fp16/bf16, two for fp32), so a
+// warp store instruction covers 1-2 KiB of contiguous output.
+//
+// Pages: "ZeRO++: Extremely Efficient Collective Communication for Large Model Training"
+// (atlas.scime.ai summary), Approach; "ZeRO++: ... Giant Model Training" (mlsanity.com),
+// Abstract: block-quantisation based all-gather.
+#include <type_traits>
+
+#include "zpp_device.cuh"
+#include "zpp_launch.h"
+
+namespace zpp {
+
+struct OutF16 {};
+struct OutBF16 {};
+struct OutF32 {};
+
+constexpr int kDqVec = 16;                 // elements per lane per row
+constexpr int kDqRow = 32 * kDqVec;        // 512
+constexpr int kDqRows = 4;
+constexpr int kDqTile = kDqRows * kDqRow;  // 2048 elements per warp tile
+
+template <int BITS>
+__device__ __forceinline__ void load_codes16(const uint8_t* p, uint32_t w[4]) {
+  if constexpr (BITS == 8) {
+    uint4 v = ld_stream_v4(p);
+    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+  } else {
+    uint2 v = ld_stream_v2(p);
+    w[0] = v.x, w[1] = v.y, w[2] = 0u, w[3] = 0u;
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ int code_of(const uint32_t w[4], int i) {
+  if constexpr (BITS == 8)
+    return code_int8(w[i >> 2], i & 3);
+  else
+    return code_int4(w[i >> 3], i & 7);
+}
+
+template <typename OT>
+__device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
+  if constexpr (std::is_same_v<OT, OutF32>) {
+    U8x32 a, b;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a.w[i] = __float_as_uint(v[i]);
+      b.w[i] = __float_as_uint(v[8 + i]);
+    }
+    float* p = static_cast<float*>(y) + e;
+    st_v8(p, a);
+    st_v8(p + 8, b);
+  } else {
+    using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
+    U8x32 a;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
+    st_v8(static_cast<uint16_t*>(y) + e, a);
+  }
+}
+
+template <typename OT>
+__device__ __forceinline__ void store1(void* y, int64_t e, float v) {
+  if constexpr (std::is_same_v<OT, OutF32>)
+    static_cast<float*>(y)[e] = v;
+  else if constexpr (std::is_same_v<OT, OutF16>)
+    static_cast<__half*>(y)[e] = __float2half_rn(v);
+  else
+    static_cast<__nv_bfloat16*>(y)[e] = __float2bfloat16_rn(v);
+}
+
+template <int BITS, typename OT>
+__global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict__ codes,
+                                                      const float* __restrict__ scales,
+                                                      int64_t n, int log2b, void* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t full = n / kDqTile;
+  for (int64_t t = gw; t < full; t += nw) {
+    uint32_t w[kDqRows][4];
+    float s[kDqRows];
+#pragma unroll
+    for (int u = 0; u < kDqRows; ++u) {
+      const int64_t e = t * kDqTile + u * kDqRow + lane * kDqVec;
+      load_codes16<BITS>(codes + e * BITS / 8, w[u]);
+      s[u] = __ldg(scales + (e >> log2b));
+    }
+#pragma unroll
+    for (int u = 0; u < kDqRows; ++u) {
+      const int64_t e = t * kDqTile + u * kDqRow + lane * kDqVec;
+      float v[kDqVec];
+#pragma unroll
+      for (int i = 0; i < kDqVec; ++i) v[i] = __fmul_rn(static_cast<float>(code_of<BITS>(w[u], i)), s[u]);
+      store16<OT>(y, e, v);
+    }
+  }
+  // Ragged end: element-wise, by the warp whose turn it would be.
+  const int64_t rem = n - full * kDqTile;
+  if (rem > 0 && gw == full % nw) {
+    for (int64_t e = full * kDqTile + lane; e < n; e += 32) {
+      const int code = BITS == 8 ? static_cast<int>(static_cast<int8_t>(__ldg(codes + e)))
+                                 : code_int4(__ldg(codes + (e >> 1)), static_cast<int>(e & 1));
+      store1<OT>(y, e, __fmul_rn(static_cast<float>(code), __ldg(scales + (e >> log2b))));
+    }
+  }
+}
+
+template <int BITS, typename OT>
+static cudaError_t run_dequant(const void* codes, const float* scales, int64_t n, int log2b,
+                               void* y, cudaStream_t s) {
+  auto kern = k_dequant<BITS, OT>;
+  static const int occ = occupancy_of(kern, kThreads);
+  const int64_t tiles = (n + kDqTile - 1) / kDqTile;
+  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(codes), scales, n, log2b, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const void* codes, const float* scales, int64_t n, int block, int bits,
+                           void* y, int out_kind, cudaStream_t s) {
+  const int log2b = __builtin_ctz(static_cast<unsigned>(block));
+  if (bits == 8) {
+    if (out_kind == 0) return run_dequant<8, OutF16>(codes, scales, n, log2b, y, s);
+    if (out_kind == 1) return run_dequant<8, OutBF16>(codes, scales, n, log2b, y, s);
+    return run_dequant<8, OutF32>(codes, scales, n, log2b, y, s);
+  }
+  if (out_kind == 0) return run_dequant<4, OutF16>(codes, scales, n, log2b, y, s);
+  if (out_kind == 1) return run_dequant<4, OutBF16>(codes, scales, n, log2b, y, s);
+  return run_dequant<4, OutF32>(codes, scales, n, log2b, y, s);
+}
+
+}  // namespace zpp

@@ -1,0 +1,247 @@
+// quant.cu -- K1 (qwZ block quantisation) and K3 (qgZ slice reorder + quantisation).
+//
+// Both run the same warp tile: a warp owns TILE = max(block, 2048) consecutive
+// elements, each lane loads 16 of them per row with one 256-bit load (a row is 512
+// elements, 1 KiB of fp16/bf16), all rows of the tile are in flight before any
+// arithmetic, the block absmax is taken on the sign-cleared 16-bit patterns (two per
+// instruction) and reduced with warp shuffles, and each lane packs its 16 codes into
+// one 16-byte (INT8) or 8-byte (INT4) store. Every input byte is read exactly once.
+//
+// Pages: "ZeRO++: Extremely Efficient Collective Communication for Large Model
+// Training" (atlas.scime.ai summary), Approach: block-wise INT8 weight quantisation,
+// INT4 gradients, tensor-slice reordering for correct placement. "LIT-102: ZeRO++ ..."
+// Key takeaways: block-wise rather than per-tensor scales.
+#include "zpp_device.cuh"
+#include "zpp_launch.h"
+
+namespace zpp {
+
+template <int B>
+struct QuantTile {
+  static constexpr int VEC = 16;                      // elements per lane per row
+  static constexpr int ROW = 32 * VEC;                // 512 elements per warp row
+  static constexpr int TILE = B > 2048 ? B : 2048;    // elements per warp tile
+  static constexpr int ROWS = TILE / ROW;
+};
+
+// Quantise one warp tile. `in` points at the tile's first input element, `codes` at its
+// first code byte, `scales` at its first block scale. FULL: all TILE elements valid;
+// otherwise only the first `valid` (any count; lanes past it load zeros, which leave
+// the absmax unchanged and give code 0, and store nothing).
+template <typename TT, int BITS, int B, bool FULL>
+__device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
+                                           uint8_t* __restrict__ codes,
+                                           float* __restrict__ scales, int valid, int lane) {
+  using T = QuantTile<B>;
+  constexpr int VEC = T::VEC, ROW = T::ROW, ROWS = T::ROWS;
+  U8x32 raw[ROWS];
+  int cnt[ROWS];
+#pragma unroll
+  for (int u = 0; u < ROWS; ++u) {
+    const int off = u * ROW + lane * VEC;
+    if (FULL) {
+      cnt[u] = VEC;
+      raw[u] = ld_stream_v8(in + off);
+    } else {
+      int c = valid - off;
+      c = c < 0 ? 0 : (c > VEC ? VEC : c);
+      cnt[u] = c;
+      if (c == VEC) {
+        raw[u] = ld_stream_v8(in + off);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) raw[u].w[k] = 0u;
+        for (int i = 0; i < c; ++i)
+          raw[u].w[i >> 1] |= static_cast<uint32_t>(__ldg(in + off + i)) << (16 * (i & 1));
+      }
+    }
+  }
+
+  // Block absmax -> scale and inverse for every row.
+  float sc[ROWS], iv[ROWS];
+  if constexpr (B < ROW) {
+    constexpr int LPB = B / VEC;  // lanes per block (4, 8 or 16)
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      uint32_t a = warp_max_u32(absmax_bits16<8>(raw[u].w), LPB);
+      block_scale<BITS>(bits16_to_float(a, TT()), sc[u], iv[u]);
+    }
+  } else {
+    constexpr int RPB = B / ROW;  // rows per block
+#pragma unroll
+    for (int b = 0; b < ROWS / RPB; ++b) {
+      uint32_t a = absmax_bits16<8>(raw[b * RPB].w);
+#pragma unroll
+      for (int i = 1; i < RPB; ++i) a = max(a, absmax_bits16<8>(raw[b * RPB + i].w));
+      a = warp_max_u32(a, 32);
+      float s, v;
+      block_scale<BITS>(bits16_to_float(a, TT()), s, v);
+#pragma unroll
+      for (int i = 0; i < RPB; ++i) {
+        sc[b * RPB + i] = s;
+        iv[b * RPB + i] = v;
+      }
+    }
+  }
+
+  // Codes: 16 per lane per row.
+#pragma unroll
+  for (int u = 0; u < ROWS; ++u) {
+    const int off = u * ROW + lane * VEC;
+    int q[VEC];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float2 f = unpack2(raw[u].w[k], TT());
+      q[2 * k] = quantize<BITS>(f.x, iv[u]);
+      q[2 * k + 1] = quantize<BITS>(f.y, iv[u]);
+    }
+    if constexpr (BITS == 8) {
+      uint2 a = pack8_int8(q), b = pack8_int8(q + 8);
+      uint4 v = make_uint4(a.x, a.y, b.x, b.y);
+      if (FULL || cnt[u] == VEC) {
+        st_v4(codes + off, v);
+      } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int i = 0; i < cnt[u]; ++i) codes[off + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+      }
+    } else {
+      uint2 v = make_uint2(pack8_int4(q), pack8_int4(q + 8));
+      if (FULL || cnt[u] == VEC) {
+        st_v2(codes + off / 2, v);
+      } else {
+        const uint32_t w[2] = {v.x, v.y};
+        const int nbytes = (cnt[u] + 1) / 2;
+        for (int i = 0; i < nbytes; ++i) codes[off / 2 + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+      }
+    }
+  }
+
+  // Scales: one lane per block.
+  if constexpr (B < ROW) {
+    constexpr int LPB = B / VEC;
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      const int e0 = u * ROW + lane * VEC;
+      if ((lane % LPB) == 0 && (FULL || e0 < valid)) scales[e0 / B] = sc[u];
+    }
+  } else {
+    constexpr int RPB = B / ROW;
+#pragma unroll
+    for (int b = 0; b < ROWS / RPB; ++b)
+      if (lane == 0 && (FULL || b * B < valid)) scales[b] = sc[b * RPB];
+  }
+}
+
+// K1: x[n] -> codes, scales. Warps walk the full tiles grid-stride; the ragged last tile
+// (if any) is done by the warp whose turn it would be.
+template <typename TT, int BITS, int B>
+__global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__ x, int64_t n,
+                                                    uint8_t* __restrict__ codes,
+                                                    float* __restrict__ scales) {
+  constexpr int TILE = QuantTile<B>::TILE;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t full = n / TILE;
+  for (int64_t t = gw; t < full; t += nw)
+    quant_tile<TT, BITS, B, true>(x + t * TILE, codes + t * (TILE * BITS / 8),
+                                  scales + t * (TILE / B), TILE, lane);
+  const int64_t rem = n - full * TILE;
+  if (rem > 0 && gw == full % nw)
+    quant_tile<TT, BITS, B, false>(x + full * TILE, codes + full * (TILE * BITS / 8),
+                                   scales + full * (TILE / B), static_cast<int>(rem), lane);
+}
+
+// K3: per source rank r, output slice position p = l_d*N + n_d holds original slice
+// j = n_d*M + l_d; the work is W*W slices of S elements, each cut into tiles (the last
+// tile of a slice may be short but always holds whole blocks).
+template <typename TT, int BITS, int B>
+__global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __restrict__ grads,
+                                                            int64_t E, int N, int M,
+                                                            uint8_t* __restrict__ codes,
+                                                            float* __restrict__ scales) {
+  constexpr int TILE = QuantTile<B>::TILE;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
+  const int64_t tps = (S + TILE - 1) / TILE;
+  const int64_t total = W * W * tps;
+  for (int64_t t = gw; t < total; t += nw) {
+    const int64_t seg = t / tps, k = t - seg * tps;
+    const int64_t r = seg / W, p = seg - r * W;
+    const int64_t l_d = p / N, n_d = p - l_d * N;
+    const int64_t j = n_d * M + l_d;
+    const int64_t in_off = r * E + j * S + k * TILE;
+    const int64_t out_off = r * E + p * S + k * TILE;
+    const int64_t rem = S - k * TILE;
+    if (rem >= TILE)
+      quant_tile<TT, BITS, B, true>(grads + in_off, codes + out_off * BITS / 8, scales + out_off / B,
+                                    TILE, lane);
+    else
+      quant_tile<TT, BITS, B, false>(grads + in_off, codes + out_off * BITS / 8,
+                                     scales + out_off / B, static_cast<int>(rem), lane);
+  }
+}
+
+template <typename TT, int BITS, int B>
+static cudaError_t run_quant(const void* x, int64_t n, void* codes, float* scales, cudaStream_t s) {
+  auto kern = k_quant<TT, BITS, B>;
+  static const int occ = occupancy_of(kern, kThreads);
+  const int64_t tiles = (n + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
+  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), n, static_cast<uint8_t*>(codes),
+                                 scales);
+  return cudaGetLastError();
+}
+
+template <typename TT, int BITS, int B>
+static cudaError_t run_reorder_quant(const void* g, int64_t E, int N, int M, void* codes,
+                                     float* scales, cudaStream_t s) {
+  auto kern = k_reorder_quant<TT, BITS, B>;
+  static const int occ = occupancy_of(kern, kThreads);
+  const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
+  const int64_t tiles = W * W * ((S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE);
+  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(g), E, N, M,
+                                 static_cast<uint8_t*>(codes), scales);
+  return cudaGetLastError();
+}
+
+// Compile-time dispatch over (dtype, bits, block).
+template <typename TT, int BITS, typename F>
+static cudaError_t by_block(int block, F&& f) {
+  switch (block) {
+    case 64: return f.template operator()<TT, BITS, 64>();
+    case 128: return f.template operator()<TT, BITS, 128>();
+    case 256: return f.template operator()<TT, BITS, 256>();
+    case 512: return f.template operator()<TT, BITS, 512>();
+    case 1024: return f.template operator()<TT, BITS, 1024>();
+    case 2048: return f.template operator()<TT, BITS, 2048>();
+    case 4096: return f.template operator()<TT, BITS, 4096>();
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename F>
+static cudaError_t by_type_bits_block(int is_bf16, int bits, int block, F&& f) {
+  if (is_bf16)
+    return bits == 8 ? by_block<BF16, 8>(block, f) : by_block<BF16, 4>(block, f);
+  return bits == 8 ? by_block<F16, 8>(block, f) : by_block<F16, 4>(block, f);
+}
+
+cudaError_t launch_quant(const void* x, int is_bf16, int64_t n, int block, int bits, void* codes,
+                         float* scales, cudaStream_t s) {
+  return by_type_bits_block(is_bf16, bits, block, [&]<typename TT, int BITS, int B>() {
+    return run_quant<TT, BITS, B>(x, n, codes, scales, s);
+  });
+}
+
+cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block, int bits,
+                                 int N, int M, void* codes, float* scales, cudaStream_t s) {
+  return by_type_bits_block(is_bf16, bits, block, [&]<typename TT, int BITS, int B>() {
+    return run_reorder_quant<TT, BITS, B>(grads, E, N, M, codes, scales, s);
+  });
+}
+
+}  // namespace zpp

@@ -1,0 +1,183 @@
+// zpp_abi.cu -- the extern "C" boundary of libzpp: argument checks (before any launch),
+// kernel selection, status codes, and the same-run 256-bit copy kernel.
+#include <zpp.h>
+
+#include "zpp_device.cuh"
+#include "zpp_launch.h"
+
+namespace zpp {
+
+int sm_count() {
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (dev < 0 || dev >= kMaxDev) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 1;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// K6: streaming copy, one 256-bit load and store per lane per step.
+__global__ void __launch_bounds__(kThreads) k_copy(const U8x32* __restrict__ src,
+                                                   U8x32* __restrict__ dst, int64_t nvec) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    U8x32 a = ld_stream_v8(src + i), b = ld_stream_v8(src + i + stride);
+    U8x32 c = ld_stream_v8(src + i + 2 * stride), d = ld_stream_v8(src + i + 3 * stride);
+    st_v8(dst + i, a);
+    st_v8(dst + i + stride, b);
+    st_v8(dst + i + 2 * stride, c);
+    st_v8(dst + i + 3 * stride, d);
+  }
+  for (; i < nvec; i += stride) st_v8(dst + i, ld_stream_v8(src + i));
+}
+
+cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s) {
+  static const int occ = occupancy_of(k_copy, kThreads);
+  const int64_t nvec = bytes / 32;
+  const int grid = persistent_grid((nvec + kThreads - 1) / kThreads, occ);
+  k_copy<<<grid, kThreads, 0, s>>>(static_cast<const U8x32*>(src), static_cast<U8x32*>(dst), nvec);
+  return cudaGetLastError();
+}
+
+}  // namespace zpp
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_block(int32_t block) {
+  return block >= ZPP_MIN_BLOCK && block <= ZPP_MAX_BLOCK && (block & (block - 1)) == 0;
+}
+
+bool valid_bits(int32_t bits) { return bits == 4 || bits == 8; }
+
+zpp_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ZPP_OK : ZPP_ERR_CUDA; }
+
+// Shared checks of the three qgZ entry points; on success W is set.
+zpp_status check_topology(int64_t E, int32_t block, int32_t bits, zpp_topology t, int64_t* W) {
+  if (!valid_bits(bits) || !valid_block(block)) return ZPP_ERR_INVALID_ARG;
+  if (t.num_nodes < 1 || t.gpus_per_node < 1) return ZPP_ERR_INVALID_ARG;
+  const int64_t w = static_cast<int64_t>(t.num_nodes) * t.gpus_per_node;
+  if (w > 65536) return ZPP_ERR_INVALID_ARG;
+  if (E < 0 || E >= (int64_t{1} << 31)) return ZPP_ERR_INVALID_ARG;
+  if (E % (w * block) != 0) return ZPP_ERR_INVALID_ARG;
+  if (w * E > ZPP_MAX_ELEMS) return ZPP_ERR_INVALID_ARG;
+  *W = w;
+  return ZPP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t zpp_code_bytes(int64_t n, int32_t bits) {
+  if (n < 0 || !valid_bits(bits)) return -1;
+  return bits == 8 ? n : (n + 1) / 2;
+}
+
+int64_t zpp_num_scales(int64_t n, int32_t block) {
+  if (n < 0 || block <= 0) return -1;
+  return (n + block - 1) / block;
+}
+
+const char* zpp_status_string(zpp_status s) {
+  switch (s) {
+    case ZPP_OK: return "ZPP_OK";
+    case ZPP_ERR_INVALID_ARG: return "ZPP_ERR_INVALID_ARG: invalid argument";
+    case ZPP_ERR_MISALIGNED: return "ZPP_ERR_MISALIGNED: pointer alignment rule broken";
+    case ZPP_ERR_UNSUPPORTED: return "ZPP_ERR_UNSUPPORTED: unsupported dtype combination";
+    case ZPP_ERR_CUDA: return "ZPP_ERR_CUDA: CUDA runtime error at launch";
+  }
+  return "unknown zpp_status";
+}
+
+zpp_status zpp_quant_blockwise(const void* x, zpp_dtype x_dt, int64_t n, int32_t block,
+                               int32_t bits, void* codes, float* scales, cudaStream_t stream) {
+  if (!valid_bits(bits) || !valid_block(block) || n < 0 || n > ZPP_MAX_ELEMS)
+    return ZPP_ERR_INVALID_ARG;
+  if (x_dt != ZPP_F16 && x_dt != ZPP_BF16 && x_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (n == 0) return ZPP_OK;
+  if (!x || !codes || !scales) return ZPP_ERR_INVALID_ARG;
+  if (x_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
+  if (!aligned(x, 32) || !aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_quant(x, x_dt == ZPP_BF16, n, block, bits, codes, scales, stream));
+}
+
+zpp_status zpp_dequant_blockwise(const void* codes, const float* scales, int64_t n, int32_t block,
+                                 int32_t bits, void* y, zpp_dtype y_dt, cudaStream_t stream) {
+  if (!valid_bits(bits) || !valid_block(block) || n < 0 || n > ZPP_MAX_ELEMS)
+    return ZPP_ERR_INVALID_ARG;
+  if (y_dt != ZPP_F16 && y_dt != ZPP_BF16 && y_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (n == 0) return ZPP_OK;
+  if (!codes || !scales || !y) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 32) || !aligned(y, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_dequant(codes, scales, n, block, bits, y, static_cast<int>(y_dt), stream));
+}
+
+zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
+                                 int32_t block, int32_t bits, zpp_topology topo, void* codes,
+                                 float* scales, cudaStream_t stream) {
+  int64_t W = 0;
+  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (g_dt != ZPP_F16 && g_dt != ZPP_BF16 && g_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0) return ZPP_OK;
+  if (!grads || !codes || !scales) return ZPP_ERR_INVALID_ARG;
+  if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
+  if (!aligned(grads, 32) || !aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_reorder_quant(grads, g_dt == ZPP_BF16, elems_per_rank, block, bits,
+                                             topo.num_nodes, topo.gpus_per_node, codes, scales,
+                                             stream));
+}
+
+zpp_status zpp_dequant_reduce_requant(const void* codes, const float* scales,
+                                      int64_t elems_per_rank, int32_t block, int32_t bits,
+                                      zpp_topology topo, void* out_codes, float* out_scales,
+                                      cudaStream_t stream) {
+  int64_t W = 0;
+  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (elems_per_rank == 0) return ZPP_OK;
+  if (!codes || !scales || !out_codes || !out_scales) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 32) || !aligned(out_codes, 32) || !aligned(scales, 4) ||
+      !aligned(out_scales, 4))
+    return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits,
+                                                      topo.num_nodes, topo.gpus_per_node,
+                                                      out_codes, out_scales, stream));
+}
+
+zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t elems_per_rank,
+                              int32_t block, int32_t bits, zpp_topology topo, float* out,
+                              cudaStream_t stream) {
+  int64_t W = 0;
+  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (elems_per_rank == 0) return ZPP_OK;
+  if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
+                                              topo.num_nodes, topo.gpus_per_node, out, stream));
+}
+
+zpp_status zpp_device_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream) {
+  if (bytes < 0 || bytes % 32 != 0) return ZPP_ERR_INVALID_ARG;
+  if (bytes == 0) return ZPP_OK;
+  if (!src || !dst) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(src, 32) || !aligned(dst, 32)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_copy(src, dst, bytes, stream));
+}
+
+}  // extern "C"

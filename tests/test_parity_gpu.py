@@ -1,0 +1,272 @@
+"""GPU parity: every kernel, called through the C ABI, against the CPU oracle on the same
+seeded inputs. Codes, scales, dequantised fp16/bf16 values and the reorder permutation
+must match bit for bit; fp32 sums (fixed ascending order, no FMA) are required within
+1e-6 relative and are expected to match exactly, which is also checked.
+
+Sizes span several warp tiles plus a ragged tail, every block size and both code widths,
+the small and the full-size workloads, and the edge cases (empty, one element, odd
+lengths, blocks longer than the data, the largest block)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_zero_communication_gb300 as zpp
+from quantized_zero_communication_gb300 import binding as zb
+from quantized_zero_communication_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+BLOCKS = (64, 128, 256, 512, 1024, 2048, 4096)
+DEV = "cuda:0"
+REL_TOL = 1e-6  # fp32 reductions
+
+
+def bits16(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def odt(dtype):
+    return {torch.float16: oracle.F16, torch.bfloat16: oracle.BF16, torch.float32: oracle.F32}[dtype]
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_f32_parity(got, want):
+    got, want = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    err = np.abs(got.astype(np.float64) - want)
+    assert np.all(err <= REL_TOL * np.abs(want.astype(np.float64)) + 1e-30), float(err.max())
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), "fp32 sums not bit-identical"
+
+
+def check_quant(x, block, bits):
+    codes, scales = zpp.quant_blockwise(x, block, bits)
+    oc, os_ = oracle.quant_blockwise(bits16(x), odt(x.dtype), block, bits)
+    assert np.array_equal(host(codes), oc)
+    assert np.array_equal(host(scales).view(np.uint32), os_.view(np.uint32))
+    return codes, scales, oc, os_
+
+
+# ----------------------------------------------------------------------- qwZ (K1, K2)
+@pytest.mark.parametrize("block", BLOCKS)
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_quant_dequant_all_blocks(block, bits, dtype):
+    n = 3 * max(block, 2048) + 5 * 16 + 7  # several warp tiles, a ragged tile, odd tail
+    kind = inputs.SWEEP_KINDS[(block + bits) % 3]
+    x = inputs.draw(kind, n, seed=block + bits, dtype=dtype, device=DEV)
+    codes, scales, oc, os_ = check_quant(x, block, bits)
+    for out_dt in (torch.float16, torch.bfloat16, torch.float32):
+        y = zpp.dequant_blockwise(codes, scales, n, block, bits, out_dt)
+        oy = oracle.dequant_blockwise(oc, os_, n, block, bits, odt(out_dt))
+        got = host(y.view(torch.int16)).view(np.uint16) if out_dt != torch.float32 else host(y)
+        assert np.array_equal(got.view(oy.dtype), oy)
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 15, 16, 17, 63, 64, 65, 511, 513, 2047, 2049, 4095, 4097,
+                               10_001])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quant_edge_lengths(n, bits):
+    for block in (64, 4096):
+        x = inputs.draw("uniform_outliers", n, seed=n, dtype=torch.float16, device=DEV)
+        codes, scales, oc, os_ = check_quant(x, block, bits)
+        y = zpp.dequant_blockwise(codes, scales, n, block, bits, torch.float16)
+        oy = oracle.dequant_blockwise(oc, os_, n, block, bits, oracle.F16)
+        assert np.array_equal(bits16(y), oy)
+
+
+def test_golden_cases_on_gpu():
+    """The hand-derived fixtures use 4-element blocks, below the ABI's minimum block of 64;
+    each fixture block is embedded at the start of its own 64-element block padded with
+    zeros, which leaves its absmax, scale and codes unchanged."""
+    from tests.golden import load_quant_cases
+    for case in load_quant_cases():
+        dt = torch.float16 if case["dtype"] == "f16" else torch.bfloat16
+        B, bits, n = case["block"], case["bits"], len(case["x"])
+        x = torch.tensor(case["x"], dtype=torch.float64).to(dt)
+        nb = -(-n // B)
+        padded = torch.zeros(nb * 64, dtype=dt)
+        for b in range(nb):
+            seg = x[b * B:(b + 1) * B]
+            padded[b * 64:b * 64 + seg.numel()] = seg
+        codes, scales = zpp.quant_blockwise(padded.to(DEV), 64, bits)
+        y = zpp.dequant_blockwise(codes, scales, nb * 64, 64, bits, dt)
+        c, yb = host(codes), bits16(y)
+        per = 64 * bits // 8
+        lens = [min(B, n - b * B) for b in range(nb)]
+        got = np.concatenate([c[b * per:b * per + (lens[b] * bits + 7) // 8] for b in range(nb)])
+        assert list(got) == case["packed"], case["name"]
+        assert list(host(scales).view(np.uint32)) == case["scale_bits"], case["name"]
+        got_y = np.concatenate([yb[b * 64:b * 64 + lens[b]] for b in range(nb)])
+        want_y = bits16(torch.tensor(case["y"], dtype=torch.float64).to(dt))
+        assert np.array_equal(got_y, want_y), case["name"]
+
+
+def test_zero_length_is_a_noop():
+    x = torch.zeros(0, dtype=torch.float16, device=DEV)
+    codes = torch.full((32,), 0xAB, dtype=torch.uint8, device=DEV)
+    scales = torch.full((8,), 3.0, device=DEV)
+    assert zb.zpp_quant_blockwise(0, zb.ZPP_F16, 0, 256, 8,
+                                  codes.data_ptr(), scales.data_ptr()) == zb.ZPP_OK
+    assert torch.all(codes == 0xAB) and torch.all(scales == 3.0)
+
+
+def test_invalid_arguments_write_nothing():
+    x = inputs.draw("normal", 4096, seed=1, dtype=torch.float16, device=DEV)
+    buf = torch.full((8192,), 0x5A, dtype=torch.uint8, device=DEV)
+    sc = torch.full((64,), -1.0, device=DEV)
+    st = zb.zpp_quant_blockwise(x.data_ptr() + 16, zb.ZPP_F16, 1024, 256, 8, buf.data_ptr(),
+                                sc.data_ptr())
+    assert st == zb.ZPP_ERR_MISALIGNED
+    st = zb.zpp_quant_blockwise(x.data_ptr(), zb.ZPP_F16, 4096, 96, 8, buf.data_ptr(), sc.data_ptr())
+    assert st == zb.ZPP_ERR_INVALID_ARG
+    st = zb.zpp_quant_blockwise(x.data_ptr(), zb.ZPP_F16, 4096, 256, 8, buf.data_ptr() + 16,
+                                sc.data_ptr())
+    assert st == zb.ZPP_ERR_MISALIGNED
+    torch.cuda.synchronize()
+    assert torch.all(buf == 0x5A) and torch.all(sc == -1.0)
+
+
+def test_shard_launches_equal_one_launch():
+    """qwZ quantises per rank; 16 shard launches at their offsets == one launch."""
+    n_shard, R, B = 2048 * 24, 16, 2048
+    x = inputs.draw("normal", n_shard * R, seed=77, dtype=torch.float16, device=DEV)
+    c_all, s_all = zpp.quant_blockwise(x, B, 8)
+    c_sh = torch.empty_like(c_all)
+    s_sh = torch.empty_like(s_all)
+    for r in range(R):
+        zpp.quant_blockwise(x[r * n_shard:(r + 1) * n_shard], B, 8,
+                            codes=c_sh[r * n_shard:(r + 1) * n_shard],
+                            scales=s_sh[r * n_shard // B:(r + 1) * n_shard // B])
+    torch.cuda.synchronize()
+    assert torch.equal(c_all, c_sh) and torch.equal(s_all, s_sh)
+
+
+def test_repeat_calls_are_deterministic():
+    x = inputs.draw("laplace", 1 << 20, seed=3, dtype=torch.bfloat16, device=DEV)
+    a = zpp.quant_blockwise(x, 512, 4)
+    b = zpp.quant_blockwise(x, 512, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_qwz_round_trip_workload():
+    x = inputs.qwz_round_trip(DEV)
+    codes, scales, oc, os_ = check_quant(x, 256, 8)
+    y = zpp.dequant_blockwise(codes, scales, x.numel(), 256, 8, torch.float16)
+    assert np.array_equal(bits16(y), oracle.dequant_blockwise(oc, os_, x.numel(), 256, 8, oracle.F16))
+
+
+# ----------------------------------------------------------------------- qgZ (K3, K4, K5)
+TOPOS = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 4), (3, 2), (4, 3), (1, 8), (1, 16), (4, 8)]
+
+
+def run_qgz(g, block, bits, N, M):
+    E = g.shape[1]
+    c0, s0 = zpp.qgz_reorder_quant(g, block, bits, N, M)
+    c1, s1 = zpp.dequant_reduce_requant(c0, s0, E, block, bits, N, M)
+    out = zpp.dequant_reduce(c1, s1, E, block, bits, N, M)
+    return [host(t) for t in (c0, s0, c1, s1, out)]
+
+
+def check_qgz(g, block, bits, N, M):
+    got = run_qgz(g, block, bits, N, M)
+    want = oracle.qgz_pipeline(bits16(g), odt(g.dtype), block, bits, N, M)
+    names = ("reordered codes", "source scales", "hop-1 codes", "hop-1 scales")
+    for a, b, name in zip(got[:4], want[:4], names):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), name
+    assert_f32_parity(got[4], want[4])
+
+
+@pytest.mark.parametrize("N,M", TOPOS)
+@pytest.mark.parametrize("bits", [4, 8])
+def test_qgz_pipeline_topologies(N, M, bits):
+    W = N * M
+    for block in (64, 512, 4096):
+        # a slice of two blocks plus one slice spanning several tiles
+        for per_slice in (2 * block, 3 * 8192 + block):
+            if W * W * per_slice > (1 << 24):
+                continue
+            E = W * per_slice
+            g = inputs.draw("laplace", W * E, seed=W + block, dtype=torch.bfloat16,
+                            device=DEV).reshape(W, E)
+            check_qgz(g, block, bits, N, M)
+
+
+def test_qgz_fp16_gradients():
+    g = inputs.draw("normal", 8 * 8 * 1024, seed=4, dtype=torch.float16, device=DEV).reshape(8, -1)
+    check_qgz(g, 128, 4, 2, 4)
+
+
+def test_qgz_tiny_workload():
+    check_qgz(inputs.qgz_tiny(DEV), 128, 4, 2, 4)
+
+
+@pytest.mark.parametrize("K", [2, 8, 16])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_dequant_reduce_requant_sweep_shapes(K, bits):
+    """The sweep's K-way fused reduction: topology {1 node, K GPUs}."""
+    for block in (64, 256, 1024, 4096):
+        E = K * block * 4
+        g = inputs.draw("uniform_outliers", K * E, seed=K * block, dtype=torch.float16,
+                        device=DEV).reshape(K, E)
+        check_qgz(g, block, bits, 1, K)
+
+
+# ----------------------------------------------------------------------- full-size workloads
+@pytest.mark.slow
+def test_gpt_layer_full_size():
+    """qwZ on one hidden-8192 GPT layer: 805,306,368 fp16 weights, INT8 block 2048,
+    quantised in one launch (16 block-aligned shards) and dequantised after the gather."""
+    x = inputs.gpt_layer(DEV)
+    n = x.numel()
+    codes, scales = zpp.quant_blockwise(x, 2048, 8)
+    y = zpp.dequant_blockwise(codes, scales, n, 2048, 8, torch.float16)
+    xb = bits16(x)
+    oc, os_ = oracle.quant_blockwise(xb, oracle.F16, 2048, 8)
+    assert np.array_equal(host(codes), oc)
+    assert np.array_equal(host(scales).view(np.uint32), os_.view(np.uint32))
+    del codes
+    oy = oracle.dequant_blockwise(oc, os_, n, 2048, 8, oracle.F16)
+    assert np.array_equal(bits16(y), oy)
+
+
+@pytest.mark.slow
+def test_gradient_bucket_full_size():
+    """qgZ on a 536,870,912-element bf16 bucket over 4 nodes x 8 GPUs, INT4 block 512."""
+    g = inputs.gradient_bucket(DEV)
+    check_qgz(g, 512, 4, 4, 8)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("bits", [8, 4])
+def test_largest_sweep_size(bits):
+    """The sweep's largest size (2^30 elements) through quant, dequant and the fused
+    K-way reduction, checked against the oracle on the whole tensor."""
+    n = 1 << 30
+    x = inputs.draw("uniform_outliers", n, seed=999, dtype=torch.bfloat16, device=DEV)
+    codes, scales, oc, os_ = check_quant(x, 4096, bits)
+    y = zpp.dequant_blockwise(codes, scales, n, 4096, bits, torch.bfloat16)
+    assert np.array_equal(bits16(y), oracle.dequant_blockwise(oc, os_, n, 4096, bits, oracle.BF16))
+    del x, y, codes, scales
+    K = 16
+    g = inputs.draw("normal", n, seed=1000, dtype=torch.bfloat16, device=DEV).reshape(K, n // K)
+    E = n // K
+    c0, s0 = zpp.qgz_reorder_quant(g, 1024, bits, 1, K)
+    c1, s1 = zpp.dequant_reduce_requant(c0, s0, E, 1024, bits, 1, K)
+    oc0, os0 = oracle.qgz_reorder_quant(bits16(g), oracle.BF16, 1024, bits, 1, K)
+    assert np.array_equal(host(c0), oc0)
+    oc1, os1 = oracle.dequant_reduce_requant(oc0, os0, E, 1024, bits, 1, K)
+    assert np.array_equal(host(c1), oc1)
+    assert np.array_equal(host(s1).view(np.uint32), os1.view(np.uint32))
+
+
+def test_device_copy():
+    a = torch.randint(0, 255, (1 << 20,), dtype=torch.uint8, device=DEV)
+    b = torch.zeros_like(a)
+    zpp.device_copy(a, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
