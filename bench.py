@@ -1,0 +1,503 @@
+"""Benchmark of the ZeRO++ block-quantisation hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  qwZ on one hidden-8192 GPT layer (805,306,368 fp16 weights, 16 virtual ranks, INT8
+  block 2048): K1 quantise, K2 dequantise the gathered codes;
+  qgZ on one gradient bucket (536,870,912 bf16 gradients over 4 nodes x 8 GPUs, INT4
+  block 512): K3 reorder + quantise, K4 fused dequant -> fp32 sum -> requant (K = 8),
+  K5 final dequant-reduce (K = 4).
+Metric: algorithmic bytes moved per second (GB/s) -- reads plus writes each kernel
+must make, summed over the step -- with the dominant kernel's fraction of the measured
+HBM bandwidth. Inputs (5.4 GB) far exceed the 129 MB L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica on its own GPU (weak scaling, no
+data-path collective); rank 0 prints one JSON line.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quant / dequant-reduce-requant GB/s and % of GB300 HBM peak (1 GPU)"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+# Workload (sizes of the qwZ GPT-layer and qgZ bucket configurations).
+QWZ_BLOCK, QWZ_BITS = 2048, 8
+QGZ_N, QGZ_M, QGZ_BLOCK, QGZ_BITS = 4, 8, 512, 4
+QGZ_ELEMS_PER_RANK = 16_777_216
+KERNELS = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant",
+           "K5_dequant_reduce")
+KERNEL_SOURCES = {"K1_quant": ["quant.cu", "zpp_device.cuh"],
+                  "K2_dequant": ["dequant.cu", "zpp_device.cuh"],
+                  "K3_reorder_quant": ["quant.cu", "zpp_device.cuh"],
+                  "K4_dequant_reduce_requant": ["qgz.cu", "zpp_device.cuh"],
+                  "K5_dequant_reduce": ["qgz.cu", "zpp_device.cuh"]}
+
+
+# ----------------------------------------------------------------------------- accounting
+def code_bytes(n, bits):
+    return n if bits == 8 else (n + 1) // 2
+
+
+def step_bytes(n_qwz, E, div=1):
+    """Algorithmic bytes per launch of each kernel (reads + writes it cannot avoid)."""
+    W, M = QGZ_N * QGZ_M, QGZ_M
+    C, S = E // M, E // W
+    qs = 4 * math.ceil(n_qwz / QWZ_BLOCK)
+    b = {
+        "K1_quant": 2 * n_qwz + code_bytes(n_qwz, QWZ_BITS) + qs,
+        "K2_dequant": code_bytes(n_qwz, QWZ_BITS) + qs + 2 * n_qwz,
+        "K3_reorder_quant": W * (2 * E + code_bytes(E, QGZ_BITS) + 4 * (E // QGZ_BLOCK)),
+        "K4_dequant_reduce_requant": W * (code_bytes(E, QGZ_BITS) + 4 * (E // QGZ_BLOCK))
+        + W * (code_bytes(C, QGZ_BITS) + 4 * (C // QGZ_BLOCK)),
+        "K5_dequant_reduce": W * (code_bytes(C, QGZ_BITS) + 4 * (C // QGZ_BLOCK)) + 4 * W * S,
+    }
+    return b
+
+
+def workload_sizes(div):
+    from quantized_zero_communication_gb300 import inputs
+    return inputs.GPT_LAYER_ELEMS // div, QGZ_ELEMS_PER_RANK // div
+
+
+def workload_config(div, n_qwz, E):
+    return {
+        "workload": "qwZ GPT layer (hidden 8192: 805,306,368 fp16 weights, 16 virtual ranks, "
+                    "INT8 block 2048) + qGZ gradient bucket (536,870,912 bf16 over 4 nodes x "
+                    "8 GPUs, INT4 block 512, K=8 then K=4)" + (f", sizes / {div}" if div > 1 else ""),
+        "qwz_elements": n_qwz, "qwz_block": QWZ_BLOCK, "qwz_bits": QWZ_BITS, "qwz_ranks": 16,
+        "qgz_elements": QGZ_N * QGZ_M * E, "qgz_topology": [QGZ_N, QGZ_M],
+        "qgz_block": QGZ_BLOCK, "qgz_bits": QGZ_BITS,
+        "l2": "inputs larger than L2 (no flush)", "parallelism": "replica per GPU",
+    }
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), \
+        int(os.environ.get("WORLD_SIZE", 1))
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    rank, _, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(value, device="cpu"):
+    """Largest `value` over all ranks (the value itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FLAGS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id, self.proc, self.file = gpu_id, None, None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu_id)], stdout=self.file,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        import datetime
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                p = [c.strip() for c in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(p[1]), float(p[2]), p[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside:  # region shorter than the sampling period: nearest samples
+            mid = (t0 + t1) / 2
+            inside = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+        sm = sorted(r[1] for r in inside)
+        reasons = sorted({name for r in inside for name, v in zip(self.FLAGS, r[3])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------- peaks
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(kernel):
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "quantized_zero_communication_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, units_ratio):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu capture, scaled to this
+    launch's size; None if no capture exists or the kernel source changed since."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_digest") != source_digest(kernel):
+        return None
+    return rec["dram_bytes_per_launch"] * units_ratio / rec.get("units_ratio", 1.0)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import quantized_zero_communication_gb300 as zpp
+    from quantized_zero_communication_gb300 import build as zbuild, inputs
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    if not os.path.exists(zbuild.LIB):
+        zbuild.build()
+    div = args.size_div
+    n_qwz, E = workload_sizes(div)
+    W, N, M = QGZ_N * QGZ_M, QGZ_N, QGZ_M
+    C, S = E // M, E // W
+    per_kernel_bytes = step_bytes(n_qwz, E)
+    bytes_step = sum(per_kernel_bytes.values())
+
+    # Inputs resident in HBM; outputs preallocated.
+    x = inputs.gpt_layer(dev, div=div)
+    g = inputs.gradient_bucket(dev, W=W, elems_per_rank=E)
+    codes = torch.empty(code_bytes(n_qwz, QWZ_BITS), dtype=torch.uint8, device=dev)
+    scales = torch.empty(math.ceil(n_qwz / QWZ_BLOCK), dtype=torch.float32, device=dev)
+    y = torch.empty(n_qwz, dtype=torch.float16, device=dev)
+    c0 = torch.empty((W, code_bytes(E, QGZ_BITS)), dtype=torch.uint8, device=dev)
+    s0 = torch.empty((W, E // QGZ_BLOCK), dtype=torch.float32, device=dev)
+    c1 = torch.empty((W, code_bytes(C, QGZ_BITS)), dtype=torch.uint8, device=dev)
+    s1 = torch.empty((W, C // QGZ_BLOCK), dtype=torch.float32, device=dev)
+    out = torch.empty((W, S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
+        if ev is not None:
+            ev[1].record(stream)
+        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
+        if ev is not None:
+            ev[2].record(stream)
+        zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
+        if ev is not None:
+            ev[3].record(stream)
+        zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
+        if ev is not None:
+            ev[4].record(stream)
+        zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
+        if ev is not None:
+            ev[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # Timed region: exactly K steps, events on the launching stream around each kernel.
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    sampler = ClockSampler(_smi_id(dev, local))
+    sampler.start()
+    time.sleep(0.15)
+    barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        step(events[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1)
+    elapsed_ms = start.elapsed_time(end)
+    max_ms = max_over_ranks(elapsed_ms, device=dev)
+    ms_per_step = max_ms / args.steps
+    value = world * bytes_step * args.steps / (max_ms * 1e-3) / 1e9
+
+    # Per-kernel durations (ms, summed over the timed steps).
+    kt = {k: 0.0 for k in KERNELS}
+    for ev in events:
+        for i, k in enumerate(KERNELS):
+            kt[k] += ev[i].elapsed_time(ev[i + 1])
+    peak, peak_src = hbm_peak()
+    kernels = {}
+    for k in KERNELS:
+        avg_s = kt[k] / args.steps * 1e-3
+        gbs = per_kernel_bytes[k] / avg_s / 1e9
+        kernels[k] = {"us": round(avg_s * 1e6, 2), "bytes": per_kernel_bytes[k],
+                      "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                      "share": round(kt[k] / sum(kt.values()), 4)}
+    dom = max(KERNELS, key=lambda k: kt[k])
+    full_bytes = step_bytes(*workload_sizes(1))[dom]
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
+            "peak_source": peak_src, "unit": "GB/s",
+            "frac": round(kernels[dom]["gbs"] / peak, 4),
+            "traffic": ncu_traffic(dom, per_kernel_bytes[dom] / full_bytes)}
+    # same-run copy kernel on 1 GiB (reference for the same HBM)
+    copy_gbs = _copy_reference(zpp, torch, dev)
+
+    result = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+              "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic (seeded N(0,0.02/sqrt(96)) fp16 weights; Laplace(0,1e-4) bf16 "
+                      "gradients with 0.01% x100 spikes)",
+              "config": workload_config(div, n_qwz, E),
+              "roofline": roof, "kernels": kernels,
+              "copy_kernel_gbs": round(copy_gbs, 1),
+              "gpu_launches": len(KERNELS) * args.steps, "clocks": clocks}
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1,
+                                out, n_qwz, E, bytes_step, world)
+    del x, g, codes, scales, y, c0, s0, c1, s1, out
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    return result
+
+
+def _smi_id(dev, local):
+    import torch
+    u = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if u is not None:
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    return str(local)
+
+
+def _copy_reference(zpp, torch, dev):
+    a = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(3):
+        zpp.device_copy(a, b)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(10):
+        zpp.device_copy(a, b)
+    e.record()
+    torch.cuda.synchronize()
+    t = s.elapsed_time(e) / 10 * 1e-3
+    del a, b
+    return 2 * (1 << 30) / t / 1e9
+
+
+def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, n_qwz, E,
+            bytes_step, world):
+    """The same step through the public API with host buffers: every step copies the
+    weights and gradients in from pinned host memory and copies the dequantised weights
+    and the reduced gradient slices back out."""
+    W, N, M = QGZ_N * QGZ_M, QGZ_N, QGZ_M
+    def pinned(t):
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+    hx, hg, hy, hout = pinned(x), pinned(g), pinned(y), pinned(out)
+    hx.copy_(x)
+    hg.copy_(g)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        x.copy_(hx, non_blocking=True)
+        g.copy_(hg, non_blocking=True)
+        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
+        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
+        zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
+        zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
+        zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
+        hy.copy_(y, non_blocking=True)
+        hout.copy_(out, non_blocking=True)
+
+    steps = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), device=dev)
+    h2d = hx.numel() * hx.element_size() + hg.numel() * hg.element_size()
+    d2h = hy.numel() * hy.element_size() + hout.numel() * hout.element_size()
+    return {"value": round(world * bytes_step * steps / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(ms / steps, 3)}
+
+
+# ----------------------------------------------------------------------------- oracle legs
+def oracle_sample_step(div, seed_cache={}):
+    """The whole path on the CPU oracle over a 1/div sample of the workload (the first
+    1/div of the layer's weights; the bucket with 1/div of the elements per rank on the
+    same 4 x 8 topology). Returns (algorithmic bytes, seconds)."""
+    import numpy as np
+    import torch
+    import oracle
+    from quantized_zero_communication_gb300 import inputs
+
+    key = div
+    if key not in seed_cache:
+        seed_cache.clear()
+        x = inputs.gpt_layer("cpu", div=div)
+        g = inputs.gradient_bucket("cpu", W=QGZ_N * QGZ_M, elems_per_rank=QGZ_ELEMS_PER_RANK // div)
+        seed_cache[key] = (x.view(torch.int16).numpy().view(np.uint16),
+                           g.view(torch.int16).numpy().view(np.uint16))
+    xb, gb = seed_cache[key]
+    n_qwz, E = xb.size, gb.shape[1]
+    t0 = time.perf_counter()
+    c, s = oracle.quant_blockwise(xb, oracle.F16, QWZ_BLOCK, QWZ_BITS)
+    oracle.dequant_blockwise(c, s, n_qwz, QWZ_BLOCK, QWZ_BITS, oracle.F16)
+    oracle.qgz_pipeline(gb, oracle.BF16, QGZ_BLOCK, QGZ_BITS, QGZ_N, QGZ_M)
+    dt = time.perf_counter() - t0
+    return sum(step_bytes(n_qwz, E).values()), dt
+
+
+def _calibrated_div(target_s):
+    """Smallest power-of-two divisor whose sample runs in about target_s seconds."""
+    div = 1024
+    b, t = oracle_sample_step(div)
+    while div > 4 and t * 2 < target_s:
+        div //= 2
+        t *= 2
+    return div
+
+
+def cpu_baseline(target_s):
+    import oracle
+    cores = oracle.set_threads(len(os.sched_getaffinity(0)))
+    div = _calibrated_div(target_s)
+    b, t = oracle_sample_step(div)
+    return {"value": round(b / t / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"1/{div} of the workload (first {1}/{div} of the layer weights; bucket "
+                      f"with {QGZ_ELEMS_PER_RANK // div} elements per rank, same topology); "
+                      f"{t:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle timed as the reference arm (rank 0 only)."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    cores = oracle.set_threads(len(os.sched_getaffinity(0)))
+    per_step = args.ref_seconds or max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    div = _calibrated_div(per_step)
+    for _ in range(args.warmup):
+        oracle_sample_step(div)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = oracle_sample_step(div)
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    n_qwz, E = workload_sizes(1)
+    sample = (f"each step 1/{div} of the workload (first 1/{div} of the layer weights; bucket "
+              f"with {QGZ_ELEMS_PER_RANK // div} elements per rank, same 4x8 topology)")
+    result = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+              "ms_per_step": round(tot_t / args.steps * 1e3, 2), "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+              "data": "synthetic (same generators and seeds as the GPU arm)",
+              "config": workload_config(1, n_qwz, E),
+              "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
+                               "kind": "oracle", "sample": sample},
+              "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                      "d2h_bytes_per_step": 0}}
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--size-div", type=int, default=1,
+                    help="shrink the workload by this power of two (profiling runs only)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=0.0,
+                    help="target seconds per reference step (default: fit the run in minutes)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.size_div < 1 or args.size_div & (args.size_div - 1) or args.size_div > 1024:
+        ap.error("--size-div must be a power of two <= 1024")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
