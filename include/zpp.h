@@ -13,11 +13,12 @@
  * reading every entry point implements, bit for bit):
  *   per block of `block` consecutive elements (the last block may be shorter):
  *     amax  = max |x|;  scale = fp32(amax / qmax);  inv = fp32(qmax / amax)
- *     q     = clamp(rint_to_even(fp32(x * inv)), -qmax, qmax),  qmax = 2^(bits-1) - 1
+ *     q     = clamp(rint_to_even(x * inv), -qmax, qmax),  qmax = 2^(bits-1) - 1,
+ *             the product x * inv taken exactly (rounded once, to an integer)
  *     amax == 0 or inv not finite  ->  scale = 0 and every q = 0
  *   dequantise: y = fp32((float)q * scale), then round-to-nearest-even into y's type.
- *   Every fp32 operation is rounded on its own (no FMA); sums start at +0.0f and add
- *   sources in ascending order.
+ *   reduce (the qgZ hops): sum = fma(q, scale, sum) per received chunk -- one rounding
+ *   per term -- starting from +0.0f, sources in ascending order.
  *
  * Storage: INT8 codes are two's-complement bytes; INT4 codes are two's-complement
  * nibbles, element 2i in the LOW nibble of byte i and 2i+1 in the high nibble (an odd

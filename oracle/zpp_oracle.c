@@ -23,13 +23,17 @@
  *   amax   = max |x| over the block
  *   qmax   = 2^(bits-1) - 1                        (127 for INT8, 7 for INT4: symmetric)
  *   scale  = amax / qmax,  inv = qmax / amax       (two IEEE fp32 divisions per block)
- *   q      = clamp(rint(x * inv), -qmax, qmax)     (rint: ties to even)
+ *   q      = clamp(rint(x * inv), -qmax, qmax)     (rint: ties to even, applied to the
+ *                                                   exact product x * inv)
  *   if amax == 0 or inv is not finite: scale = 0, q = 0 for the whole block
  *   y      = (float) q * scale                     (then RNE cast to the output type)
+ *   sum    = fma(q, scale, sum) per received chunk (one rounding per term; sums start at
+ *                                                   +0.0f, sources in ascending order)
  *
- * Every fp32 operation is rounded on its own (the file is compiled with
- * -ffp-contract=off and without fast-math), reductions run in ascending source order
- * starting from +0.0f. INT4 codes are two's-complement nibbles, element 2i in the low
+ * The products x * inv are formed exactly in double (24-bit by 24-bit significands fit in
+ * 53 bits) and rounded to an integer once; the hop sums add each dequantised term with a
+ * single rounding (C99 fmaf). Nothing else is fused: the file is compiled with
+ * -ffp-contract=off and without fast-math. INT4 codes are two's-complement nibbles, element 2i in the low
  * nibble of byte i, element 2i+1 in the high nibble; a trailing odd element leaves the
  * high nibble 0. Scales are a separate fp32 array, one per block.
  *
@@ -155,7 +159,7 @@ static void quant_block(const float* v, int64_t len, int bits, int8_t* q, float*
     return;
   }
   for (int64_t i = 0; i < len; ++i) {
-    float t = nearbyintf(v[i] * inv);
+    double t = nearbyint((double)v[i] * (double)inv); /* exact product, one rounding */
     if (t > qmax) t = qmax;
     if (t < -qmax) t = -qmax;
     q[i] = (int8_t)t;
@@ -286,8 +290,8 @@ int or_qgz_reorder_quant(const void* grads, int dtype, int64_t E, int64_t block,
 }
 
 /* Step a5 (hop 1 + the fused kernel of the pages): receiver (n, l) dequantises chunk l
- * of each rank (n, l'), sums in fp32 over l' = 0..M-1 ascending from +0.0f, then
- * requantises the N*S sums by blocks.
+ * of each rank (n, l'), sums in fp32 over l' = 0..M-1 ascending from +0.0f (each term
+ * q * scale added with one rounding), then requantises the N*S sums by blocks.
  * codes/scales: the output of step a3. out_codes [W][code_bytes(N*S)], out_scales
  * [W][N*S/block]. */
 int or_dequant_reduce_requant(const uint8_t* codes, const float* scales, int64_t E,
@@ -305,9 +309,8 @@ int or_dequant_reduce_requant(const uint8_t* codes, const float* scales, int64_t
         for (int lp = 0; lp < M; ++lp) {
           int64_t src = hop1_source(n, M, lp);
           int64_t idx = (int64_t)l * C + e; /* chunk l of the reordered source */
-          float d = (float)code_at(codes + src * or_code_bytes(E, bits), bits, idx) *
-                    scales[src * (E / block) + idx / block];
-          a = a + d;
+          a = fmaf((float)code_at(codes + src * or_code_bytes(E, bits), bits, idx),
+                   scales[src * (E / block) + idx / block], a);
         }
         acc[e] = a;
       }
@@ -323,8 +326,8 @@ int or_dequant_reduce_requant(const uint8_t* codes, const float* scales, int64_t
 }
 
 /* Step a7 (hop 2): receiver (n, l) dequantises slice n of the hop-1 output of every rank
- * (n', l) and sums over n' = 0..N-1 ascending from +0.0f. out [W][S] fp32 (a sum; any
- * averaging factor is left to the caller). */
+ * (n', l) and sums over n' = 0..N-1 ascending from +0.0f (one rounding per term).
+ * out [W][S] fp32 (a sum; any averaging factor is left to the caller). */
 int or_dequant_reduce(const uint8_t* codes1, const float* scales1, int64_t E, int64_t block,
                       int bits, int N, int M, float* out) {
   int64_t W = (int64_t)N * M, S = E / W, C = (int64_t)N * S;
@@ -337,9 +340,8 @@ int or_dequant_reduce(const uint8_t* codes1, const float* scales1, int64_t E, in
         for (int np = 0; np < N; ++np) {
           int64_t src = hop2_source(np, M, l);
           int64_t idx = (int64_t)n * S + e; /* slice n of the hop-1 output */
-          float d = (float)code_at(codes1 + src * or_code_bytes(C, bits), bits, idx) *
-                    scales1[src * (C / block) + idx / block];
-          a = a + d;
+          a = fmaf((float)code_at(codes1 + src * or_code_bytes(C, bits), bits, idx),
+                   scales1[src * (C / block) + idx / block], a);
         }
         out[r * S + e] = a;
       }

@@ -36,22 +36,42 @@ __device__ __forceinline__ void load_codes16(const uint8_t* p, uint32_t w[4]) {
   }
 }
 
+// 16 codes -> 8 pairs of dequantised fp32 values, y = fl((float)q * s).
 template <int BITS>
-__device__ __forceinline__ int code_of(const uint32_t w[4], int i) {
-  if constexpr (BITS == 8)
-    return code_int8(w[i >> 2], i & 3);
-  else
-    return code_int4(w[i >> 3], i & 7);
+__device__ __forceinline__ void dequant16(const uint32_t w[4], float s, f32x2 v[8]) {
+  const f32x2 ss = f2(s, s);
+  if constexpr (BITS == 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f32x2 q[2];
+      int8x4_to_f2(w[k], q);
+      v[2 * k] = f2_mul(q[0], ss);
+      v[2 * k + 1] = f2_mul(q[1], ss);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      f32x2 q[4];
+      int4x8_to_f2(w[k], q);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[4 * k + j] = f2_mul(q[j], ss);
+    }
+  }
 }
 
 template <typename OT>
-__device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
+__device__ __forceinline__ void store16(void* y, int64_t e, const f32x2 v[8]) {
   if constexpr (std::is_same_v<OT, OutF32>) {
     U8x32 a, b;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      a.w[i] = __float_as_uint(v[i]);
-      b.w[i] = __float_as_uint(v[8 + i]);
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      f2_split(v[i], lo, hi);
+      a.w[2 * i] = __float_as_uint(lo);
+      a.w[2 * i + 1] = __float_as_uint(hi);
+      f2_split(v[4 + i], lo, hi);
+      b.w[2 * i] = __float_as_uint(lo);
+      b.w[2 * i + 1] = __float_as_uint(hi);
     }
     float* p = static_cast<float*>(y) + e;
     st_v8(p, a);
@@ -60,7 +80,11 @@ __device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
     using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
     U8x32 a;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
+    for (int i = 0; i < 8; ++i) {
+      float lo, hi;
+      f2_split(v[i], lo, hi);
+      a.w[i] = pack2(lo, hi, TT());
+    }
     st_v8(static_cast<uint16_t*>(y) + e, a);
   }
 }
@@ -95,9 +119,8 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
 #pragma unroll
     for (int u = 0; u < kDqRows; ++u) {
       const int64_t e = t * kDqTile + u * kDqRow + lane * kDqVec;
-      float v[kDqVec];
-#pragma unroll
-      for (int i = 0; i < kDqVec; ++i) v[i] = __fmul_rn(static_cast<float>(code_of<BITS>(w[u], i)), s[u]);
+      f32x2 v[kDqVec / 2];
+      dequant16<BITS>(w[u], s[u], v);
       store16<OT>(y, e, v);
     }
   }

@@ -17,11 +17,51 @@
 
 namespace zpp {
 
+// acc (pairs of fp32 sums) += dequantised 16 code bytes with scale s: each term q * s is
+// added with one rounding (fused multiply-add), in the order the sources are visited.
 template <int BITS>
-__device__ __forceinline__ float dq(const uint4& v, int i, float s) {
-  const uint32_t w = (&v.x)[BITS == 8 ? (i >> 2) : (i >> 3)];
-  const int q = BITS == 8 ? code_int8(w, i & 3) : code_int4(w, i & 7);
-  return __fmul_rn(static_cast<float>(q), s);
+__device__ __forceinline__ void accumulate16B(f32x2* acc, const uint4& v, float s) {
+  const f32x2 ss = f2(s, s);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (BITS == 8) {
+      f32x2 q[2];
+      int8x4_to_f2(w[k], q);
+      acc[2 * k] = f2_fma(q[0], ss, acc[2 * k]);
+      acc[2 * k + 1] = f2_fma(q[1], ss, acc[2 * k + 1]);
+    } else {
+      f32x2 q[4];
+      int4x8_to_f2(w[k], q);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[4 * k + j] = f2_fma(q[j], ss, acc[4 * k + j]);
+    }
+  }
+}
+
+// acc += dequantised 8 code bytes (INT4: 16 codes) or 16 code bytes (INT8: 16 codes).
+template <int BITS>
+__device__ __forceinline__ void accumulate16codes(f32x2* acc, const uint4& v, float s) {
+  const f32x2 ss = f2(s, s);
+  if constexpr (BITS == 8) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f32x2 q[2];
+      int8x4_to_f2(w[k], q);
+      acc[2 * k] = f2_fma(q[0], ss, acc[2 * k]);
+      acc[2 * k + 1] = f2_fma(q[1], ss, acc[2 * k + 1]);
+    }
+  } else {
+    const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      f32x2 q[4];
+      int4x8_to_f2(w[k], q);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[4 * k + j] = f2_fma(q[j], ss, acc[4 * k + j]);
+    }
+  }
 }
 
 // K4. CTA tile: 8 warps x one row each; a row is 32 lanes x EPL elements (one 16-byte
@@ -52,9 +92,10 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
     const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx * BITS / 8;
     const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
-    float acc[EPL];
+    constexpr int NP = EPL / 2;  // fp32 pairs per lane
+    f32x2 acc[NP];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < NP; ++j) acc[j] = f2(0.0f, 0.0f);
     for (int k0 = 0; k0 < M; k0 += KC) {
       uint4 raw[KC];
       float s[KC];
@@ -70,15 +111,16 @@ __global__ void __launch_bounds__(kThreads)
       }
 #pragma unroll
       for (int i = 0; i < KC; ++i) {
-        if (k0 + i < M) {
-#pragma unroll
-          for (int j = 0; j < EPL; ++j) acc[j] = __fadd_rn(acc[j], dq<BITS>(raw[i], j, s[i]));
-        }
+        if (k0 + i < M) accumulate16B<BITS>(acc, raw[i], s[i]);
       }
     }
     float m = 0.0f;
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) m = fmaxf(m, fabsf(acc[j]));
+    for (int j = 0; j < NP; ++j) {
+      float a, b;
+      f2_split(acc[j], a, b);
+      m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+    }
     if (B <= ROWLEN) {
       m = warp_max(m, B / EPL);
     } else {
@@ -93,16 +135,20 @@ __global__ void __launch_bounds__(kThreads)
     float sc, iv;
     block_scale<BITS>(m, sc, iv);
     if (valid) {
-      int q[EPL];
+      const f32x2 iv2 = f2(iv, iv);
+      uint32_t w[4];
 #pragma unroll
-      for (int j = 0; j < EPL; ++j) q[j] = quantize<BITS>(acc[j], iv);
-      uint4 v;
-      if constexpr (BITS == 8) {
-        uint2 a = pack8_int8(q), b = pack8_int8(q + 8);
-        v = make_uint4(a.x, a.y, b.x, b.y);
-      } else {
-        v = make_uint4(pack8_int4(q), pack8_int4(q + 8), pack8_int4(q + 16), pack8_int4(q + 24));
+      for (int k = 0; k < 4; ++k) {
+        if constexpr (BITS == 8) {
+          const f32x2 r[2] = {round_codes(acc[2 * k], iv2), round_codes(acc[2 * k + 1], iv2)};
+          w[k] = pack_int8x4(r);
+        } else {
+          const f32x2 r[4] = {round_codes(acc[4 * k], iv2), round_codes(acc[4 * k + 1], iv2),
+                              round_codes(acc[4 * k + 2], iv2), round_codes(acc[4 * k + 3], iv2)};
+          w[k] = pack_int4x8(r);
+        }
       }
+      const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
       st_v4(out_codes + r * cb_out + e * BITS / 8, v);
       if ((e & (B - 1)) == 0) out_scales[r * sc_out + (e >> log2b)] = sc;
     }
@@ -132,9 +178,9 @@ __global__ void __launch_bounds__(kThreads)
     const uint8_t* cbase = codes + static_cast<int64_t>(l) * cb + idx * BITS / 8;
     const float* sbase = scales + static_cast<int64_t>(l) * sc + (idx >> log2b);
     const int64_t cstep = static_cast<int64_t>(M) * cb, sstep = static_cast<int64_t>(M) * sc;
-    float acc[EPL];
+    f32x2 acc[EPL / 2];
 #pragma unroll
-    for (int j = 0; j < EPL; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < EPL / 2; ++j) acc[j] = f2(0.0f, 0.0f);
     for (int k0 = 0; k0 < N; k0 += KC) {
       uint4 raw[KC];
       float s[KC];
@@ -155,21 +201,19 @@ __global__ void __launch_bounds__(kThreads)
       }
 #pragma unroll
       for (int i = 0; i < KC; ++i) {
-        if (k0 + i < N) {
-#pragma unroll
-          for (int j = 0; j < EPL; ++j) {
-            const uint32_t w = BITS == 8 ? (&raw[i].x)[j >> 2] : (&raw[i].x)[j >> 3];
-            const int q = BITS == 8 ? code_int8(w, j & 3) : code_int4(w, j & 7);
-            acc[j] = __fadd_rn(acc[j], __fmul_rn(static_cast<float>(q), s[i]));
-          }
-        }
+        if (k0 + i < N) accumulate16codes<BITS>(acc, raw[i], s[i]);
       }
     }
     U8x32 a, b;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      a.w[j] = __float_as_uint(acc[j]);
-      b.w[j] = __float_as_uint(acc[8 + j]);
+    for (int j = 0; j < 4; ++j) {
+      float lo, hi;
+      f2_split(acc[j], lo, hi);
+      a.w[2 * j] = __float_as_uint(lo);
+      a.w[2 * j + 1] = __float_as_uint(hi);
+      f2_split(acc[4 + j], lo, hi);
+      b.w[2 * j] = __float_as_uint(lo);
+      b.w[2 * j + 1] = __float_as_uint(hi);
     }
     float* p = out + r * S + e;
     st_v8(p, a);

@@ -84,20 +84,20 @@ __device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
     }
   }
 
-  // Codes: 16 per lane per row.
+  // Codes: 16 per lane per row, rounded with the magic-number addition (see round_codes).
 #pragma unroll
   for (int u = 0; u < ROWS; ++u) {
     const int off = u * ROW + lane * VEC;
-    int q[VEC];
+    const f32x2 iv2 = f2(iv[u], iv[u]);
+    f32x2 r[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      float2 f = unpack2(raw[u].w[k], TT());
-      q[2 * k] = quantize<BITS>(f.x, iv[u]);
-      q[2 * k + 1] = quantize<BITS>(f.y, iv[u]);
+      const float2 f = unpack2(raw[u].w[k], TT());
+      r[k] = round_codes(f2(f.x, f.y), iv2);
     }
     if constexpr (BITS == 8) {
-      uint2 a = pack8_int8(q), b = pack8_int8(q + 8);
-      uint4 v = make_uint4(a.x, a.y, b.x, b.y);
+      const uint4 v = make_uint4(pack_int8x4(r), pack_int8x4(r + 2), pack_int8x4(r + 4),
+                                 pack_int8x4(r + 6));
       if (FULL || cnt[u] == VEC) {
         st_v4(codes + off, v);
       } else {
@@ -105,7 +105,7 @@ __device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
         for (int i = 0; i < cnt[u]; ++i) codes[off + i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
       }
     } else {
-      uint2 v = make_uint2(pack8_int4(q), pack8_int4(q + 8));
+      const uint2 v = make_uint2(pack_int4x8(r), pack_int4x8(r + 4));
       if (FULL || cnt[u] == VEC) {
         st_v2(codes + off / 2, v);
       } else {

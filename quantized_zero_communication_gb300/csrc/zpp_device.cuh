@@ -2,10 +2,10 @@
 // 256-bit global vector accesses, 16-bit float unpacking, absmax, and the block
 // quantiser's per-element arithmetic.
 //
-// Numerics: every fp32 operation uses an explicitly rounded intrinsic (__fmul_rn,
-// __fadd_rn, __fdiv_rn, __float2int_rn), so no multiply-add is ever contracted into an
-// FMA and each division is the IEEE one; the build also passes -fmad=false and keeps
-// denormals (no -ftz).
+// Numerics: every fp32 operation is an explicitly rounded one (paired add.rn/mul.rn,
+// __fadd_rn, __fmul_rn, __fdiv_rn), so no multiply-add is ever contracted into an FMA
+// and each division is the IEEE one; integer<->float conversions use exact magic-number
+// identities (below). The build also passes -fmad=false and keeps denormals (no -ftz).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -135,35 +135,116 @@ __device__ __forceinline__ void block_scale(float amax, float& scale, float& inv
   }
 }
 
-// q = clamp(rint_even(x * inv), -qmax, qmax)
-template <int BITS>
-__device__ __forceinline__ int quantize(float x, float inv) {
-  int q = __float2int_rn(__fmul_rn(x, inv));
-  q = max(q, -QParams<BITS>::qmax);
-  return min(q, QParams<BITS>::qmax);
-}
-
-// Pack eight signed codes: INT8 -> two words (byte i = code i); INT4 -> one word
-// (nibble i = code i, so element 2k is the low nibble of byte k).
-__device__ __forceinline__ uint2 pack8_int8(const int* q) {
-  uint2 r;
-  r.x = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) | ((uint32_t)q[3] << 24);
-  r.y = (q[4] & 0xff) | ((q[5] & 0xff) << 8) | ((q[6] & 0xff) << 16) | ((uint32_t)q[7] << 24);
-  return r;
-}
-__device__ __forceinline__ uint32_t pack8_int4(const int* q) {
-  uint32_t r = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) r |= (static_cast<uint32_t>(q[i]) & 0xfu) << (4 * i);
-  return r;
-}
-
 // Signed code i of a packed word (sign-extended by arithmetic shifts).
 __device__ __forceinline__ int code_int8(uint32_t w, int i) {
   return static_cast<int>(w << (24 - 8 * i)) >> 24;
 }
 __device__ __forceinline__ int code_int4(uint32_t w, int i) {
   return static_cast<int>(w << (28 - 4 * i)) >> 28;
+}
+
+// ---------------------------------------------------------------------------------
+// Paired fp32 arithmetic (sm_100 and later): one instruction applies the same IEEE
+// single-precision operation to two independent lanes, each rounded to nearest even
+// (no flush to zero). A product that feeds a sum is always written as the explicit
+// fused form f2_fma (one rounding): the assembler may fuse a paired multiply followed
+// by a paired add even when both carry .rn, so the two-step form is never relied on.
+// ---------------------------------------------------------------------------------
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// a * b + c per lane, computed exactly and rounded once.
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ---------------------------------------------------------------------------------
+// Exact integer <-> float conversions without the conversion unit.
+//
+// Code -> float: a code q offset to an unsigned u = q + 2^(bits-1) is byte-permuted into
+// the low mantissa bits of 2^23, giving exactly 2^23 + u; subtracting 2^23 + 2^(bits-1)
+// (exact: both operands are integers below 2^24) leaves exactly (float)q.
+//
+// Float -> code: for a real t with |t| < 2^22, fl(t + 1.5*2^23) lies in [2^23, 2^24),
+// where the fp32 spacing is 1, so rounding the sum rounds t to the nearest integer with
+// ties to even (1.5*2^23 is even); the bit pattern is 0x4B400000 + rint(t), whose low
+// byte is rint(t) in two's complement. With t = x * inv formed inside one fused
+// multiply-add, this is rint of the exact product.
+// ---------------------------------------------------------------------------------
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+// Byte j (0..3) of w placed in the mantissa of 2^23: bits 0x4B0000bb.
+__device__ __forceinline__ float byte_to_magic(uint32_t w, int j) {
+  return __uint_as_float(__byte_perm(w, 0x4B00u, 0x5440u + j));
+}
+
+// Eight INT4 codes (one word, element i in nibble i) -> four pairs (2j, 2j+1) of floats.
+__device__ __forceinline__ void int4x8_to_f2(uint32_t w, f32x2 q[4]) {
+  const uint32_t lo = (w ^ 0x88888888u) & 0x0F0F0F0Fu;         // codes 0,2,4,6 (+8)
+  const uint32_t hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;  // codes 1,3,5,7 (+8)
+  const f32x2 off = f2(-8388616.0f, -8388616.0f);               // -(2^23 + 8)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) q[j] = f2_add(f2(byte_to_magic(lo, j), byte_to_magic(hi, j)), off);
+}
+
+// Four INT8 codes (one word, element i in byte i) -> two pairs of floats.
+__device__ __forceinline__ void int8x4_to_f2(uint32_t w, f32x2 q[2]) {
+  const uint32_t u = w ^ 0x80808080u;  // q + 128 in every byte
+  const f32x2 off = f2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  q[0] = f2_add(f2(byte_to_magic(u, 0), byte_to_magic(u, 1)), off);
+  q[1] = f2_add(f2(byte_to_magic(u, 2), byte_to_magic(u, 3)), off);
+}
+
+// Low bytes of four rounded magic floats (as bits) -> one word [q0, q1, q2, q3].
+__device__ __forceinline__ uint32_t gather_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040u), __byte_perm(c, d, 0x0040u), 0x5410u);
+}
+
+// Eight rounded magic floats (pairs (0,1),(2,3),(4,5),(6,7)) -> one INT4 word.
+__device__ __forceinline__ uint32_t pack_int4x8(const f32x2 r[4]) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) f2_split(r[j], v[2 * j], v[2 * j + 1]);
+  const uint32_t ev = gather_low_bytes(__float_as_uint(v[0]), __float_as_uint(v[2]),
+                                       __float_as_uint(v[4]), __float_as_uint(v[6]));
+  const uint32_t od = gather_low_bytes(__float_as_uint(v[1]), __float_as_uint(v[3]),
+                                       __float_as_uint(v[5]), __float_as_uint(v[7]));
+  return (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+}
+
+// Four rounded magic floats (pairs (0,1),(2,3)) -> one INT8 word.
+__device__ __forceinline__ uint32_t pack_int8x4(const f32x2 r[2]) {
+  float v[4];
+  f2_split(r[0], v[0], v[1]);
+  f2_split(r[1], v[2], v[3]);
+  return gather_low_bytes(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3]));
+}
+
+// Codes of a pair: rint(x * inv) of the exact product, as magic floats. No clamp is
+// needed: whenever inv is finite, |x| <= amax and inv <= (qmax / amax)(1 + 2^-24), so
+// |x * inv| <= qmax (1 + 2^-24), which rounds to at most qmax.
+__device__ __forceinline__ f32x2 round_codes(f32x2 x, f32x2 inv2) {
+  return f2_fma(x, inv2, f2(kRoundMagic, kRoundMagic));
 }
 
 __device__ __forceinline__ float warp_max(float v, int width) {

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from quantized_zero_communication_gb300 import inputs
-from tests.golden import load_quant_cases
+from tests.golden import load_qgz_case, load_quant_cases
 
 U = 2.0 ** -24  # unit roundoff of fp32
 
@@ -372,3 +372,40 @@ def test_single_rank_requant_is_idempotent():
     assert np.all(rel <= 2 * U)
     y = oracle.dequant_blockwise(c1[0], s1[0], g.shape[1], 256, 4, oracle.F32)
     assert np.array_equal(out[0], y)
+
+
+def qgz_case_inputs(case):
+    W, E = case["N"] * case["M"], case["elems_per_rank"]
+    g = torch.zeros((W, E), dtype=torch.float64)
+    for r, e, v in case["x"]:
+        g[r, e] = v
+    dt = torch.float16 if case["dtype"] == "f16" else torch.bfloat16
+    gt = g.to(dt)
+    assert torch.equal(gt.double(), g)
+    return gt
+
+
+def check_qgz_case(case, c0, s0, c1, s1, out):
+    """Compare pipeline outputs with the sparse expectations of a fixture."""
+    bits = case["bits"]
+    for r, b, want in case["source_scale_bits"]:
+        assert int(np.asarray(s0)[r, b:b + 1].view(np.uint32)[0]) == want
+    for r, e, want in case["hop1_codes"]:
+        assert unpack_codes(np.asarray(c1)[r], e + 1, bits)[e] == want
+    for r, b, want in case["hop1_scale_bits"]:
+        assert int(np.asarray(s1)[r, b:b + 1].view(np.uint32)[0]) == want
+    o = np.asarray(out).copy()
+    for r, e, want in case["out_bits"]:
+        assert int(o[r, e:e + 1].view(np.uint32)[0]) == want, (r, e)
+        o[r, e] = 0
+    assert np.all(o == 0)
+
+
+def test_golden_qgz_fused_sum():
+    """Hand-derived 1x2 pipeline: each dequantised term enters the fp32 sum with one
+    rounding (the fixture records the separately rounded alternative it excludes)."""
+    case = load_qgz_case()
+    g = qgz_case_inputs(case)
+    dt = oracle.F16 if case["dtype"] == "f16" else oracle.BF16
+    res = oracle.qgz_pipeline(bits16(g), dt, case["block"], case["bits"], case["N"], case["M"])
+    check_qgz_case(case, *res)

@@ -201,6 +201,15 @@ def test_qgz_fp16_gradients():
     check_qgz(g, 128, 4, 2, 4)
 
 
+def test_golden_qgz_fused_sum_on_gpu():
+    from tests.golden import load_qgz_case
+    from tests.test_oracle_pins import check_qgz_case, qgz_case_inputs
+    case = load_qgz_case()
+    g = qgz_case_inputs(case).to(DEV)
+    got = run_qgz(g, case["block"], case["bits"], case["N"], case["M"])
+    check_qgz_case(case, *got)
+
+
 def test_qgz_tiny_workload():
     check_qgz(inputs.qgz_tiny(DEV), 128, 4, 2, 4)
 
