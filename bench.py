@@ -234,31 +234,50 @@ def run_ours(args):
     out = torch.empty((W, S), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    B = {"x": x, "g": g, "codes": codes, "scales": scales, "y": y, "c0": c0, "s0": s0,
+         "c1": c1, "s1": s1, "out": out}
+    calls = {
+        "K1_quant": lambda: zpp.quant_blockwise(B["x"], QWZ_BLOCK, QWZ_BITS, B["codes"], B["scales"]),
+        "K2_dequant": lambda: zpp.dequant_blockwise(B["codes"], B["scales"], n_qwz, QWZ_BLOCK,
+                                                    QWZ_BITS, y=B["y"]),
+        "K3_reorder_quant": lambda: zpp.qgz_reorder_quant(B["g"], QGZ_BLOCK, QGZ_BITS, N, M,
+                                                          B["c0"], B["s0"]),
+        "K4_dequant_reduce_requant": lambda: zpp.dequant_reduce_requant(
+            B["c0"], B["s0"], E, QGZ_BLOCK, QGZ_BITS, N, M, B["c1"], B["s1"]),
+        "K5_dequant_reduce": lambda: zpp.dequant_reduce(B["c1"], B["s1"], E, QGZ_BLOCK, QGZ_BITS,
+                                                        N, M, B["out"]),
+    }
+    uses = {"K1_quant": ("x", "codes", "scales"), "K2_dequant": ("codes", "scales", "y"),
+            "K3_reorder_quant": ("g", "c0", "s0"), "K4_dequant_reduce_requant": ("c0", "s0", "c1", "s1"),
+            "K5_dequant_reduce": ("c1", "s1", "out")}
+    active = KERNELS
+    if args.only:
+        for k in KERNELS:  # one pass fills every intermediate, then keep the kernel's own
+            calls[k]()
+        torch.cuda.synchronize()
+        active = tuple(k for k in KERNELS if k.startswith(args.only))
+        del x, g, codes, scales, y, c0, s0, c1, s1, out
+        for name in list(B):
+            if name not in uses[active[0]]:
+                del B[name]
+        torch.cuda.empty_cache()
+        bytes_step = sum(per_kernel_bytes[k] for k in active)
+
     def step(ev=None):
+        for i, k in enumerate(active):
+            if ev is not None:
+                ev[i].record(stream)
+            calls[k]()
         if ev is not None:
-            ev[0].record(stream)
-        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
-        if ev is not None:
-            ev[1].record(stream)
-        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
-        if ev is not None:
-            ev[2].record(stream)
-        zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
-        if ev is not None:
-            ev[3].record(stream)
-        zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
-        if ev is not None:
-            ev[4].record(stream)
-        zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
-        if ev is not None:
-            ev[5].record(stream)
+            ev[len(active)].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
     # Timed region: exactly K steps, events on the launching stream around each kernel.
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(active) + 1)]
+              for _ in range(args.steps)]
     sampler = ClockSampler(_smi_id(dev, local))
     sampler.start()
     time.sleep(0.15)
@@ -280,26 +299,26 @@ def run_ours(args):
     value = world * bytes_step * args.steps / (max_ms * 1e-3) / 1e9
 
     # Per-kernel durations (ms, summed over the timed steps).
-    kt = {k: 0.0 for k in KERNELS}
+    kt = {k: 0.0 for k in active}
     for ev in events:
-        for i, k in enumerate(KERNELS):
+        for i, k in enumerate(active):
             kt[k] += ev[i].elapsed_time(ev[i + 1])
     peak, peak_src = hbm_peak()
     kernels = {}
-    for k in KERNELS:
+    for k in active:
         avg_s = kt[k] / args.steps * 1e-3
         gbs = per_kernel_bytes[k] / avg_s / 1e9
         kernels[k] = {"us": round(avg_s * 1e6, 2), "bytes": per_kernel_bytes[k],
                       "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                       "share": round(kt[k] / sum(kt.values()), 4)}
-    dom = max(KERNELS, key=lambda k: kt[k])
+    dom = max(active, key=lambda k: kt[k])
     full_bytes = step_bytes(*workload_sizes(1))[dom]
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
             "peak_source": peak_src, "unit": "GB/s",
             "frac": round(kernels[dom]["gbs"] / peak, 4),
             "traffic": ncu_traffic(dom, per_kernel_bytes[dom] / full_bytes)}
     # same-run copy kernel on 1 GiB (reference for the same HBM)
-    copy_gbs = _copy_reference(zpp, torch, dev)
+    copy_gbs = None if args.only else _copy_reference(zpp, torch, dev)
 
     result = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -308,14 +327,18 @@ def run_ours(args):
                       "gradients with 0.01% x100 spikes)",
               "config": workload_config(div, n_qwz, E),
               "roofline": roof, "kernels": kernels,
-              "copy_kernel_gbs": round(copy_gbs, 1),
-              "gpu_launches": len(KERNELS) * args.steps, "clocks": clocks}
-    if not args.no_e2e:
+              "copy_kernel_gbs": round(copy_gbs, 1) if copy_gbs else None,
+              "gpu_launches": len(active) * args.steps, "clocks": clocks}
+    if args.only:
+        result["only"] = active[0]
+    if not args.no_e2e and not args.only:
         result["e2e"] = run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1,
                                 out, n_qwz, E, bytes_step, world)
-    del x, g, codes, scales, y, c0, s0, c1, s1, out
+    B.clear()
+    if not args.only:
+        del x, g, codes, scales, y, c0, s0, c1, s1, out
     torch.cuda.empty_cache()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.only:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -420,24 +443,33 @@ def oracle_sample_step(div, seed_cache={}):
 
 
 def _calibrated_div(target_s):
-    """Smallest power-of-two divisor whose sample runs in about target_s seconds."""
+    """Smallest power-of-two divisor (>= 1) whose sample runs in about target_s seconds,
+    and the time one such sample is predicted to take."""
     div = 1024
     b, t = oracle_sample_step(div)
-    while div > 4 and t * 2 < target_s:
+    while div > 1 and t * 2 < target_s:
         div //= 2
         t *= 2
-    return div
+    return div, t
 
 
 def cpu_baseline(target_s):
+    """The oracle, as it stands, on all host cores over a bounded sample of the workload:
+    a 1/div slice, repeated when even the whole workload takes less than target_s."""
     import oracle
     cores = oracle.set_threads(len(os.sched_getaffinity(0)))
-    div = _calibrated_div(target_s)
-    b, t = oracle_sample_step(div)
-    return {"value": round(b / t / 1e9, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"1/{div} of the workload (first {1}/{div} of the layer weights; bucket "
-                      f"with {QGZ_ELEMS_PER_RANK // div} elements per rank, same topology); "
-                      f"{t:.1f} s"}
+    div, t_pred = _calibrated_div(target_s)
+    reps = max(1, int(target_s / max(t_pred, 1e-3))) if div == 1 else 1
+    tot_b, tot_t = 0, 0.0
+    for _ in range(reps):
+        b, t = oracle_sample_step(div)
+        tot_b += b
+        tot_t += t
+    what = "the whole workload" if div == 1 else (
+        f"1/{div} of the workload (first 1/{div} of the layer weights; bucket with "
+        f"{QGZ_ELEMS_PER_RANK // div} elements per rank, same topology)")
+    return {"value": round(tot_b / tot_t / 1e9, 3), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"{what}, {reps} pass(es), {tot_t:.1f} s"}
 
 
 def run_reference(args):
@@ -448,7 +480,7 @@ def run_reference(args):
     import oracle
     cores = oracle.set_threads(len(os.sched_getaffinity(0)))
     per_step = args.ref_seconds or max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
-    div = _calibrated_div(per_step)
+    div, _ = _calibrated_div(per_step)
     for _ in range(args.warmup):
         oracle_sample_step(div)
     tot_b, tot_t = 0, 0.0
@@ -482,6 +514,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--size-div", type=int, default=1,
                     help="shrink the workload by this power of two (profiling runs only)")
+    ap.add_argument("--only", choices=("K1", "K2", "K3", "K4", "K5"),
+                    help="time one kernel of the step on the full workload, keeping only its "
+                         "own buffers on the device (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

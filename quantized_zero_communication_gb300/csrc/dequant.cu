@@ -1,7 +1,7 @@
 // dequant.cu -- K2: qwZ dequantisation after the all-gather, y = (float)q * scale rounded
 // into fp16, bf16 or fp32.
 //
-// Warp tile: 4 rows of 512 elements. Per row a lane reads 16 codes (16 bytes INT8, 8
+// Warp tile (one per warp): 4 rows of 512 elements. Per row a lane reads 16 codes (16 bytes INT8, 8
 // bytes INT4) and one block scale (the 16 elements never straddle a block, block >= 64)
 // and writes 16 outputs with 256-bit stores (one for fp16/bf16, two for fp32), so a
 // warp store instruction covers 1-2 KiB of contiguous output.
@@ -36,17 +36,17 @@ __device__ __forceinline__ void load_codes16(const uint8_t* p, uint32_t w[4]) {
   }
 }
 
-// 16 codes -> 8 pairs of dequantised fp32 values, y = fl((float)q * s).
+// 16 codes -> 16 dequantised fp32 values in element order, y = fl((float)q * s).
 template <int BITS>
-__device__ __forceinline__ void dequant16(const uint32_t w[4], float s, f32x2 v[8]) {
+__device__ __forceinline__ void dequant16(const uint32_t w[4], float s, float v[16]) {
   const f32x2 ss = f2(s, s);
   if constexpr (BITS == 8) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       f32x2 q[2];
       int8x4_to_f2(w[k], q);
-      v[2 * k] = f2_mul(q[0], ss);
-      v[2 * k + 1] = f2_mul(q[1], ss);
+      f2_split(f2_mul(q[0], ss), v[4 * k], v[4 * k + 1]);
+      f2_split(f2_mul(q[1], ss), v[4 * k + 2], v[4 * k + 3]);
     }
   } else {
 #pragma unroll
@@ -54,24 +54,19 @@ __device__ __forceinline__ void dequant16(const uint32_t w[4], float s, f32x2 v[
       f32x2 q[4];
       int4x8_to_f2(w[k], q);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[4 * k + j] = f2_mul(q[j], ss);
+      for (int j = 0; j < 4; ++j) f2_split(f2_mul(q[j], ss), v[8 * k + 2 * j], v[8 * k + 2 * j + 1]);
     }
   }
 }
 
 template <typename OT>
-__device__ __forceinline__ void store16(void* y, int64_t e, const f32x2 v[8]) {
+__device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
   if constexpr (std::is_same_v<OT, OutF32>) {
     U8x32 a, b;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float lo, hi;
-      f2_split(v[i], lo, hi);
-      a.w[2 * i] = __float_as_uint(lo);
-      a.w[2 * i + 1] = __float_as_uint(hi);
-      f2_split(v[4 + i], lo, hi);
-      b.w[2 * i] = __float_as_uint(lo);
-      b.w[2 * i + 1] = __float_as_uint(hi);
+    for (int i = 0; i < 8; ++i) {
+      a.w[i] = __float_as_uint(v[i]);
+      b.w[i] = __float_as_uint(v[8 + i]);
     }
     float* p = static_cast<float*>(y) + e;
     st_v8(p, a);
@@ -80,11 +75,7 @@ __device__ __forceinline__ void store16(void* y, int64_t e, const f32x2 v[8]) {
     using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
     U8x32 a;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float lo, hi;
-      f2_split(v[i], lo, hi);
-      a.w[i] = pack2(lo, hi, TT());
-    }
+    for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
     st_v8(static_cast<uint16_t*>(y) + e, a);
   }
 }
@@ -104,10 +95,9 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
                                                       const float* __restrict__ scales,
                                                       int64_t n, int log2b, void* __restrict__ y) {
   const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t full = n / kDqTile;
-  for (int64_t t = gw; t < full; t += nw) {
+  if (t < full) {
     uint32_t w[kDqRows][4];
     float s[kDqRows];
 #pragma unroll
@@ -119,14 +109,12 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
 #pragma unroll
     for (int u = 0; u < kDqRows; ++u) {
       const int64_t e = t * kDqTile + u * kDqRow + lane * kDqVec;
-      f32x2 v[kDqVec / 2];
+      float v[kDqVec];
       dequant16<BITS>(w[u], s[u], v);
       store16<OT>(y, e, v);
     }
-  }
-  // Ragged end: element-wise, by the warp whose turn it would be.
-  const int64_t rem = n - full * kDqTile;
-  if (rem > 0 && gw == full % nw) {
+  } else if (t == full) {
+    // Ragged end: element-wise.
     for (int64_t e = full * kDqTile + lane; e < n; e += 32) {
       const int code = BITS == 8 ? static_cast<int>(static_cast<int8_t>(__ldg(codes + e)))
                                  : code_int4(__ldg(codes + (e >> 1)), static_cast<int>(e & 1));
@@ -139,9 +127,8 @@ template <int BITS, typename OT>
 static cudaError_t run_dequant(const void* codes, const float* scales, int64_t n, int log2b,
                                void* y, cudaStream_t s) {
   auto kern = k_dequant<BITS, OT>;
-  static const int occ = occupancy_of(kern, kThreads);
   const int64_t tiles = (n + kDqTile - 1) / kDqTile;
-  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  const int grid = tile_grid(tiles, kWarps);
   kern<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(codes), scales, n, log2b, y);
   return cudaGetLastError();
 }

@@ -132,29 +132,29 @@ __device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
   }
 }
 
-// K1: x[n] -> codes, scales. Warps walk the full tiles grid-stride; the ragged last tile
-// (if any) is done by the warp whose turn it would be.
+// K1: x[n] -> codes, scales. One warp tile per warp (a grid of one tile per warp streams
+// HBM better on this part than a persistent grid-stride loop); the warp that owns the
+// ragged last tile takes the bounds-checked path.
 template <typename TT, int BITS, int B>
 __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__ x, int64_t n,
                                                     uint8_t* __restrict__ codes,
                                                     float* __restrict__ scales) {
   constexpr int TILE = QuantTile<B>::TILE;
   const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t full = n / TILE;
-  for (int64_t t = gw; t < full; t += nw)
+  if (t < full) {
     quant_tile<TT, BITS, B, true>(x + t * TILE, codes + t * (TILE * BITS / 8),
                                   scales + t * (TILE / B), TILE, lane);
-  const int64_t rem = n - full * TILE;
-  if (rem > 0 && gw == full % nw)
-    quant_tile<TT, BITS, B, false>(x + full * TILE, codes + full * (TILE * BITS / 8),
-                                   scales + full * (TILE / B), static_cast<int>(rem), lane);
+  } else if (t == full && n > full * TILE) {
+    quant_tile<TT, BITS, B, false>(x + t * TILE, codes + t * (TILE * BITS / 8),
+                                   scales + t * (TILE / B), static_cast<int>(n - t * TILE), lane);
+  }
 }
 
 // K3: per source rank r, output slice position p = l_d*N + n_d holds original slice
-// j = n_d*M + l_d; the work is W*W slices of S elements, each cut into tiles (the last
-// tile of a slice may be short but always holds whole blocks).
+// j = n_d*M + l_d. Grid (tile group, p, r): each warp owns one warp tile of slice p of
+// rank r (the last tile of a slice may be short but always holds whole blocks).
 template <typename TT, int BITS, int B>
 __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __restrict__ grads,
                                                             int64_t E, int N, int M,
@@ -162,16 +162,12 @@ __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __re
                                                             float* __restrict__ scales) {
   constexpr int TILE = QuantTile<B>::TILE;
   const int lane = threadIdx.x & 31;
-  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
-  const int64_t tps = (S + TILE - 1) / TILE;
-  const int64_t total = W * W * tps;
-  for (int64_t t = gw; t < total; t += nw) {
-    const int64_t seg = t / tps, k = t - seg * tps;
-    const int64_t r = seg / W, p = seg - r * W;
-    const int64_t l_d = p / N, n_d = p - l_d * N;
-    const int64_t j = n_d * M + l_d;
+  const int p = blockIdx.y, r = blockIdx.z;
+  if (k * TILE < S) {
+    const int l_d = p / N, n_d = p - l_d * N;
+    const int64_t j = static_cast<int64_t>(n_d) * M + l_d;
     const int64_t in_off = r * E + j * S + k * TILE;
     const int64_t out_off = r * E + p * S + k * TILE;
     const int64_t rem = S - k * TILE;
@@ -187,9 +183,8 @@ __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __re
 template <typename TT, int BITS, int B>
 static cudaError_t run_quant(const void* x, int64_t n, void* codes, float* scales, cudaStream_t s) {
   auto kern = k_quant<TT, BITS, B>;
-  static const int occ = occupancy_of(kern, kThreads);
   const int64_t tiles = (n + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
-  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  const int grid = tile_grid(tiles, kWarps);
   kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(x), n, static_cast<uint8_t*>(codes),
                                  scales);
   return cudaGetLastError();
@@ -199,10 +194,9 @@ template <typename TT, int BITS, int B>
 static cudaError_t run_reorder_quant(const void* g, int64_t E, int N, int M, void* codes,
                                      float* scales, cudaStream_t s) {
   auto kern = k_reorder_quant<TT, BITS, B>;
-  static const int occ = occupancy_of(kern, kThreads);
   const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
-  const int64_t tiles = W * W * ((S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE);
-  const int grid = persistent_grid((tiles + kWarps - 1) / kWarps, occ);
+  const int64_t tps = (S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
+  const dim3 grid(tile_grid(tps, kWarps), static_cast<unsigned>(W), static_cast<unsigned>(W));
   kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(g), E, N, M,
                                  static_cast<uint8_t*>(codes), scales);
   return cudaGetLastError();

@@ -7,46 +7,23 @@
 
 namespace zpp {
 
-int sm_count() {
-  constexpr int kMaxDev = 64;
-  static int cache[kMaxDev] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
-  if (dev < 0 || dev >= kMaxDev) return 1;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = 1;
-    }
-    cache[dev] = n;
-  }
-  return cache[dev];
-}
-
-// K6: streaming copy, one 256-bit load and store per lane per step.
+// K6: streaming copy. Each CTA copies 4 x 256 consecutive 32-byte vectors (all loads
+// in flight before the stores) and exits.
 __global__ void __launch_bounds__(kThreads) k_copy(const U8x32* __restrict__ src,
                                                    U8x32* __restrict__ dst, int64_t nvec) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    U8x32 a = ld_stream_v8(src + i), b = ld_stream_v8(src + i + stride);
-    U8x32 c = ld_stream_v8(src + i + 2 * stride), d = ld_stream_v8(src + i + 3 * stride);
-    st_v8(dst + i, a);
-    st_v8(dst + i + stride, b);
-    st_v8(dst + i + 2 * stride, c);
-    st_v8(dst + i + 3 * stride, d);
-  }
-  for (; i < nvec; i += stride) st_v8(dst + i, ld_stream_v8(src + i));
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * 4 + threadIdx.x;
+  U8x32 r[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (base + u * kThreads < nvec) r[u] = ld_stream_v8(src + base + u * kThreads);
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    if (base + u * kThreads < nvec) st_v8(dst + base + u * kThreads, r[u]);
 }
 
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s) {
-  static const int occ = occupancy_of(k_copy, kThreads);
   const int64_t nvec = bytes / 32;
-  const int grid = persistent_grid((nvec + kThreads - 1) / kThreads, occ);
+  const int grid = tile_grid(nvec, kThreads * 4);
   k_copy<<<grid, kThreads, 0, s>>>(static_cast<const U8x32*>(src), static_cast<U8x32*>(dst), nvec);
   return cudaGetLastError();
 }
@@ -70,7 +47,7 @@ zpp_status check_topology(int64_t E, int32_t block, int32_t bits, zpp_topology t
   if (!valid_bits(bits) || !valid_block(block)) return ZPP_ERR_INVALID_ARG;
   if (t.num_nodes < 1 || t.gpus_per_node < 1) return ZPP_ERR_INVALID_ARG;
   const int64_t w = static_cast<int64_t>(t.num_nodes) * t.gpus_per_node;
-  if (w > 65536) return ZPP_ERR_INVALID_ARG;
+  if (w > 65535) return ZPP_ERR_INVALID_ARG;  // ranks index grid dimensions
   if (E < 0 || E >= (int64_t{1} << 31)) return ZPP_ERR_INVALID_ARG;
   if (E % (w * block) != 0) return ZPP_ERR_INVALID_ARG;
   if (w * E > ZPP_MAX_ELEMS) return ZPP_ERR_INVALID_ARG;

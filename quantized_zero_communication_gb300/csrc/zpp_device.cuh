@@ -180,10 +180,6 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
 // ---------------------------------------------------------------------------------
 // Exact integer <-> float conversions without the conversion unit.
 //
-// Code -> float: a code q offset to an unsigned u = q + 2^(bits-1) is byte-permuted into
-// the low mantissa bits of 2^23, giving exactly 2^23 + u; subtracting 2^23 + 2^(bits-1)
-// (exact: both operands are integers below 2^24) leaves exactly (float)q.
-//
 // Float -> code: for a real t with |t| < 2^22, fl(t + 1.5*2^23) lies in [2^23, 2^24),
 // where the fp32 spacing is 1, so rounding the sum rounds t to the nearest integer with
 // ties to even (1.5*2^23 is even); the bit pattern is 0x4B400000 + rint(t), whose low
@@ -192,12 +188,16 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
 // ---------------------------------------------------------------------------------
 constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
 
-// Byte j (0..3) of w placed in the mantissa of 2^23: bits 0x4B0000bb.
-__device__ __forceinline__ float byte_to_magic(uint32_t w, int j) {
+// Code -> float: a code q offset to an unsigned u = q + 2^(bits-1) is byte-permuted into
+// the low mantissa bits of 2^23, giving exactly 2^23 + u; subtracting 2^23 + 2^(bits-1)
+// (exact: both operands are integers below 2^24) leaves exactly (float)q. (Measured on
+// GB300 against shift + int-to-float conversion and against fp16-mantissa variants with
+// mixed-precision adds, this is the highest-throughput form.)
+__device__ __forceinline__ float byte_to_magic(uint32_t w, int j) {  // bits 0x4B0000bb
   return __uint_as_float(__byte_perm(w, 0x4B00u, 0x5440u + j));
 }
 
-// Eight INT4 codes (one word, element i in nibble i) -> four pairs (2j, 2j+1) of floats.
+// Eight INT4 codes (element i in nibble i) -> four pairs (2j, 2j+1) of exact floats.
 __device__ __forceinline__ void int4x8_to_f2(uint32_t w, f32x2 q[4]) {
   const uint32_t lo = (w ^ 0x88888888u) & 0x0F0F0F0Fu;         // codes 0,2,4,6 (+8)
   const uint32_t hi = ((w >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;  // codes 1,3,5,7 (+8)
@@ -206,9 +206,9 @@ __device__ __forceinline__ void int4x8_to_f2(uint32_t w, f32x2 q[4]) {
   for (int j = 0; j < 4; ++j) q[j] = f2_add(f2(byte_to_magic(lo, j), byte_to_magic(hi, j)), off);
 }
 
-// Four INT8 codes (one word, element i in byte i) -> two pairs of floats.
+// Four INT8 codes (element i in byte i) -> two pairs (0,1), (2,3) of exact floats.
 __device__ __forceinline__ void int8x4_to_f2(uint32_t w, f32x2 q[2]) {
-  const uint32_t u = w ^ 0x80808080u;  // q + 128 in every byte
+  const uint32_t u = w ^ 0x80808080u;              // q + 128 in every byte
   const f32x2 off = f2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
   q[0] = f2_add(f2(byte_to_magic(u, 0), byte_to_magic(u, 1)), off);
   q[1] = f2_add(f2(byte_to_magic(u, 2), byte_to_magic(u, 3)), off);

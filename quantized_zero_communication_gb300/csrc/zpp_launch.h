@@ -7,9 +7,6 @@
 
 namespace zpp {
 
-// Streaming multiprocessors of the current device (cached per device).
-int sm_count();
-
 // K1: block quantisation of n fp16 (is_bf16 = 0) or bf16 values.
 cudaError_t launch_quant(const void* x, int is_bf16, int64_t n, int block, int bits,
                          void* codes, float* scales, cudaStream_t s);
@@ -35,22 +32,12 @@ cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_
 // K6: 256-bit device copy (the same-run HBM reference).
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s);
 
-// Grid size for a persistent kernel: enough CTAs to fill every SM at the kernel's
-// occupancy, never more than there is work for.
-inline int persistent_grid(int64_t work_ctas, int ctas_per_sm) {
-  int64_t full = static_cast<int64_t>(sm_count()) * (ctas_per_sm > 0 ? ctas_per_sm : 1);
-  int64_t g = work_ctas < full ? work_ctas : full;
+// Grid size when every CTA owns `per_cta` consecutive tiles and exits (no grid-stride
+// loop): on GB300 a streaming kernel launched this way sustains more HBM bandwidth than
+// a persistent grid sized to the SM count.
+inline int tile_grid(int64_t tiles, int per_cta) {
+  int64_t g = (tiles + per_cta - 1) / per_cta;
   return static_cast<int>(g > 0 ? g : 1);
-}
-
-template <typename Kernel>
-int occupancy_of(Kernel k, int threads, size_t smem = 0) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, threads, smem) != cudaSuccess) {
-    cudaGetLastError();
-    n = 1;
-  }
-  return n > 0 ? n : 1;
 }
 
 }  // namespace zpp

@@ -99,6 +99,7 @@ def test_qgz_entry_points_reject_bad_topologies():
     for f in fns:
         assert f(8 * 128, 128, 4, T(0, 4)) == zb.ZPP_ERR_INVALID_ARG     # N < 1
         assert f(8 * 128, 128, 4, T(2, 0)) == zb.ZPP_ERR_INVALID_ARG     # M < 1
+        assert f(65536 * 64, 64, 4, T(256, 256)) == zb.ZPP_ERR_INVALID_ARG  # W > 65535
         assert f(8 * 128 + 128, 128, 4, T(2, 4)) == zb.ZPP_ERR_INVALID_ARG  # E % (W*B)
         assert f(8 * 128, 128, 6, T(2, 4)) == zb.ZPP_ERR_INVALID_ARG     # bits
         assert f(8 * 96, 96, 4, T(2, 4)) == zb.ZPP_ERR_INVALID_ARG       # block not 2^k
