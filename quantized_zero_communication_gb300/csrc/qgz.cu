@@ -7,8 +7,8 @@
 // K5 (inter-node hop): receiver (n, l) reads slice n of the hop-1 output of ranks
 // (n', l), n' = 0..N-1, dequantises and sums into its fp32 owner slice.
 //
-// A lane owns 16 consecutive elements of its receiver (8 code bytes per source for INT4,
-// 16 for INT8); its sums live in registers as eight fp32 pairs (2j, 2j+1).
+// A K4 lane reads 16 code bytes per source (32 INT4 or 16 INT8 elements); a K5 lane owns
+// 16 elements. Sums live in registers as fp32 pairs (2j, 2j+1).
 //
 // Pages: "ZeRO++: Extremely Efficient Collective Communication for Large Model Training"
 // (atlas.scime.ai summary), Approach: 2-hop all-to-all INT4 gradient reduction that
@@ -20,39 +20,32 @@
 
 namespace zpp {
 
-constexpr int kEpl = 16;               // elements per lane
-constexpr int kRow = 32 * kEpl;        // 512 elements per warp row
-constexpr int kCta = kWarps * kRow;    // 4096 elements per CTA tile
-
-// 16 codes of one lane (INT4: words x, y; INT8: x, y, z, w).
+// Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
+// in K5; a CTA tile is 8 warps x one row.
 template <int BITS>
-__device__ __forceinline__ uint4 load_codes(const uint8_t* p) {
-  if constexpr (BITS == 8) {
-    return ld_stream_v4(p);
-  } else {
-    const uint2 h = ld_stream_v2(p);
-    return make_uint4(h.x, h.y, 0u, 0u);
-  }
-}
+struct Geo4 {
+  static constexpr int EPL = BITS == 4 ? 32 : 16;  // elements per lane
+  static constexpr int ROW = 32 * EPL;
+  static constexpr int CTA = kWarps * ROW;
+  static constexpr int NP = EPL / 2;                // fp32 pairs per lane
+};
+constexpr int kEpl5 = 16;
+constexpr int kRow5 = 32 * kEpl5;
+constexpr int kCta5 = kWarps * kRow5;
 
-// acc (eight fp32 pairs) += q * s for the lane's 16 codes: each term added with one
-// rounding (fused multiply-add), in the order the sources are visited.
-template <int BITS>
-__device__ __forceinline__ void accumulate(f32x2 acc[8], const uint4& v, float s) {
+// acc (fp32 pairs (2j, 2j+1)) += q * s for the 16 code bytes of one source: each term
+// added with one rounding (fused multiply-add), in the order the sources are visited.
+template <int BITS, int NWORDS>
+__device__ __forceinline__ void accumulate(f32x2* acc, const uint32_t* w, float s) {
   const f32x2 ss = f2(s, s);
-  if constexpr (BITS == 8) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < NWORDS; ++k) {
+    if constexpr (BITS == 8) {
       f32x2 q[2];
       int8x4_to_f2(w[k], q);
       acc[2 * k] = f2_fma(q[0], ss, acc[2 * k]);
       acc[2 * k + 1] = f2_fma(q[1], ss, acc[2 * k + 1]);
-    }
-  } else {
-    const uint32_t w[2] = {v.x, v.y};
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    } else {
       f32x2 q[4];
       int4x8_to_f2(w[k], q);
 #pragma unroll
@@ -61,21 +54,47 @@ __device__ __forceinline__ void accumulate(f32x2 acc[8], const uint4& v, float s
   }
 }
 
-// The lane's 16 values in element order.
-__device__ __forceinline__ void unpair(const f32x2 acc[8], float out[16]) {
+// Sum over K sources at a constant stride, KC loads in flight per chunk. EXACT: K is a
+// multiple of KC (no per-source test); LIVE: this lane has data (else it loads nothing).
+template <int BITS, int NWORDS, int KC, bool EXACT>
+__device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase, int64_t cstep,
+                                               const float* sbase, int64_t sstep, int K, bool live) {
+  for (int k0 = 0; k0 < K; k0 += KC) {
+    uint32_t raw[KC][NWORDS];
+    float s[KC];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) f2_split(acc[j], out[2 * j], out[2 * j + 1]);
+    for (int i = 0; i < KC; ++i) {
+      if (live && (EXACT || k0 + i < K)) {
+        const uint8_t* p = cbase + (k0 + i) * cstep;
+        if constexpr (NWORDS == 4) {
+          const uint4 v = ld_stream_v4(p);
+          raw[i][0] = v.x, raw[i][1] = v.y, raw[i][2 % NWORDS] = v.z, raw[i][3 % NWORDS] = v.w;
+        } else {
+          const uint2 v = ld_stream_v2(p);
+          raw[i][0] = v.x, raw[i][1 % NWORDS] = v.y;
+        }
+        s[i] = __ldg(sbase + (k0 + i) * sstep);
+      } else {
+#pragma unroll
+        for (int k = 0; k < NWORDS; ++k) raw[i][k] = 0u;
+        s[i] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < KC; ++i)
+      if (EXACT || k0 + i < K) accumulate<BITS, NWORDS>(acc, raw[i], s[i]);
+  }
 }
 
-// K4. Grid (tile, l, n): CTA (x, l, n) owns tile x of receiver (n, l) -- 8 warps x one
-// 512-element row each -- so no thread divides to find its work. Blocks wider than a row
-// are reduced across the warps that share them through shared memory.
-template <int BITS, int KC>
-__global__ void __launch_bounds__(kThreads)
-    k_dequant_reduce_requant(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
-                             int64_t E, int log2b, int N, int M, uint8_t* __restrict__ out_codes,
-                             float* __restrict__ out_scales) {
-  __shared__ float red[kWarps];
+// K4. Grid (tile, l, n): CTA (x, l, n) owns tile x of receiver (n, l) -- 8 warps x one row
+// each -- so no thread divides to find its work. Blocks wider than a row are reduced
+// across the warps that share them through shared memory.
+template <int BITS, int KC, bool EXACT, bool FULL>
+__device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
+                                         const float* __restrict__ scales, int64_t E, int log2b,
+                                         int M, uint8_t* __restrict__ out_codes,
+                                         float* __restrict__ out_scales, float* red) {
+  using G = Geo4<BITS>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = 1 << log2b;
   const int l = blockIdx.y, n = blockIdx.z;
@@ -83,47 +102,31 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t C = E / M;  // = N * S, the hop-1 chunk
   const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
   const int64_t cb_out = C * BITS / 8, sc_out = C >> log2b;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kCta + warp * kRow + lane * kEpl;
-  const bool valid = e < C;  // C is a multiple of the block: whole blocks are in or out
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * G::CTA + warp * G::ROW + lane * G::EPL;
+  const bool valid = FULL || e < C;  // C is a multiple of the block: whole blocks in or out
   const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
   const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx * BITS / 8;
   const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
 
-  f32x2 acc[8];
+  f32x2 acc[G::NP];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = f2(0.0f, 0.0f);
-  for (int k0 = 0; k0 < M; k0 += KC) {
-    uint4 raw[KC];
-    float s[KC];
-#pragma unroll
-    for (int i = 0; i < KC; ++i) {
-      if (valid && k0 + i < M) {
-        raw[i] = load_codes<BITS>(cbase + (k0 + i) * cb_in);
-        s[i] = __ldg(sbase + (k0 + i) * sc_in);
-      } else {
-        raw[i] = make_uint4(0u, 0u, 0u, 0u);
-        s[i] = 0.0f;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < KC; ++i)
-      if (k0 + i < M) accumulate<BITS>(acc, raw[i], s[i]);
-  }
+  for (int j = 0; j < G::NP; ++j) acc[j] = f2(0.0f, 0.0f);
+  reduce_sources<BITS, 4, KC, EXACT>(acc, cbase, cb_in, sbase, sc_in, M, valid);
 
   float m = 0.0f;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < G::NP; ++j) {
     float a, b;
     f2_split(acc[j], a, b);
     m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
   }
-  if (B <= kRow) {
-    m = warp_max(m, B / kEpl);
+  if (B <= G::ROW) {
+    m = warp_max(m, B / G::EPL);
   } else {
     m = warp_max(m, 32);
     if (lane == 0) red[warp] = m;
     __syncthreads();
-    const int wpb = B / kRow, w0 = warp & ~(wpb - 1);
+    const int wpb = B / G::ROW, w0 = warp & ~(wpb - 1);
     m = red[w0];
     for (int i = 1; i < wpb; ++i) m = fmaxf(m, red[w0 + i]);
   }
@@ -131,74 +134,67 @@ __global__ void __launch_bounds__(kThreads)
   block_scale<BITS>(m, sc, iv);
   if (!valid) return;
   const f32x2 iv2 = f2(iv, iv);
-  uint8_t* dst = out_codes + r * cb_out + e * BITS / 8;
-  if constexpr (BITS == 8) {
-    uint32_t w[4];
+  uint32_t w[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < 4; ++k) {
+    if constexpr (BITS == 8) {
       const f32x2 q[2] = {round_codes(acc[2 * k], iv2), round_codes(acc[2 * k + 1], iv2)};
       w[k] = pack_int8x4(q);
-    }
-    st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-  } else {
-    uint32_t w[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    } else {
       const f32x2 q[4] = {round_codes(acc[4 * k], iv2), round_codes(acc[4 * k + 1], iv2),
                           round_codes(acc[4 * k + 2], iv2), round_codes(acc[4 * k + 3], iv2)};
       w[k] = pack_int4x8(q);
     }
-    st_v2(dst, make_uint2(w[0], w[1]));
   }
+  st_v4(out_codes + r * cb_out + e * BITS / 8, make_uint4(w[0], w[1], w[2], w[3]));
   if ((e & (B - 1)) == 0) out_scales[r * sc_out + (e >> log2b)] = sc;
+}
+
+template <int BITS, int KC, bool EXACT>
+__global__ void __launch_bounds__(kThreads)
+    k_dequant_reduce_requant(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                             int64_t E, int log2b, int M, uint8_t* __restrict__ out_codes,
+                             float* __restrict__ out_scales) {
+  __shared__ float red[kWarps];
+  const int64_t C = E / M;
+  if ((static_cast<int64_t>(blockIdx.x) + 1) * Geo4<BITS>::CTA <= C)  // CTA-uniform
+    drr_tile<BITS, KC, EXACT, true>(codes, scales, E, log2b, M, out_codes, out_scales, red);
+  else
+    drr_tile<BITS, KC, EXACT, false>(codes, scales, E, log2b, M, out_codes, out_scales, red);
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
 // slice and writes them as two 256-bit stores (each a full 32-byte sector).
-template <int BITS, int KC>
+template <int BITS, int KC, bool EXACT>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t E,
                      int log2b, int N, int M, float* __restrict__ out) {
+  constexpr int NW = BITS == 8 ? 4 : 2;  // code words per lane per source
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = blockIdx.y, n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
   const int64_t W = static_cast<int64_t>(N) * M;
   const int64_t S = E / W, C = E / M;
   const int64_t cb = C * BITS / 8, sc = C >> log2b;  // per hop-1 rank
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * kCta + warp * kRow + lane * kEpl;
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * kCta5 + warp * kRow5 + lane * kEpl5;
   if (e >= S) return;  // no barrier in this kernel
   const int64_t idx = static_cast<int64_t>(n) * S + e;  // slice n of each hop-1 output
   const uint8_t* cbase = codes + static_cast<int64_t>(l) * cb + idx * BITS / 8;
   const float* sbase = scales + static_cast<int64_t>(l) * sc + (idx >> log2b);
-  const int64_t cstep = static_cast<int64_t>(M) * cb, sstep = static_cast<int64_t>(M) * sc;
 
   f32x2 acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = f2(0.0f, 0.0f);
-  for (int k0 = 0; k0 < N; k0 += KC) {
-    uint4 raw[KC];
-    float s[KC];
-#pragma unroll
-    for (int i = 0; i < KC; ++i) {
-      if (k0 + i < N) {
-        raw[i] = load_codes<BITS>(cbase + (k0 + i) * cstep);
-        s[i] = __ldg(sbase + (k0 + i) * sstep);
-      } else {
-        raw[i] = make_uint4(0u, 0u, 0u, 0u);
-        s[i] = 0.0f;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < KC; ++i)
-      if (k0 + i < N) accumulate<BITS>(acc, raw[i], s[i]);
-  }
-  float v[16];
-  unpair(acc, v);
+  reduce_sources<BITS, NW, KC, EXACT>(acc, cbase, static_cast<int64_t>(M) * cb, sbase,
+                                      static_cast<int64_t>(M) * sc, N, true);
   U8x32 a, b;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    a.w[j] = __float_as_uint(v[j]);
-    b.w[j] = __float_as_uint(v[8 + j]);
+  for (int j = 0; j < 4; ++j) {
+    float lo, hi;
+    f2_split(acc[j], lo, hi);
+    a.w[2 * j] = __float_as_uint(lo), a.w[2 * j + 1] = __float_as_uint(hi);
+    f2_split(acc[4 + j], lo, hi);
+    b.w[2 * j] = __float_as_uint(lo), b.w[2 * j + 1] = __float_as_uint(hi);
   }
   float* p = out + r * S + e;
   st_v8(p, a);
@@ -210,11 +206,13 @@ static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1))
 template <int BITS, int KC>
 static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int log2b, int N,
                            int M, void* out_codes, float* out_scales, cudaStream_t s) {
-  const int64_t C = E / M;
-  const dim3 grid(tile_grid(C, kCta), M, N);
-  k_dequant_reduce_requant<BITS, KC><<<grid, kThreads, 0, s>>>(
-      static_cast<const uint8_t*>(codes), scales, E, log2b, N, M, static_cast<uint8_t*>(out_codes),
-      out_scales);
+  const dim3 grid(tile_grid(E / M, Geo4<BITS>::CTA), M, N);
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  uint8_t* oc = static_cast<uint8_t*>(out_codes);
+  if (M % KC == 0)
+    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, oc, out_scales);
+  else
+    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, oc, out_scales);
   return cudaGetLastError();
 }
 
@@ -222,9 +220,12 @@ template <int BITS, int KC>
 static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int log2b, int N,
                           int M, float* out, cudaStream_t s) {
   const int64_t S = E / (static_cast<int64_t>(N) * M);
-  const dim3 grid(tile_grid(S, kCta), M, N);
-  k_dequant_reduce<BITS, KC><<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(codes), scales,
-                                                       E, log2b, N, M, out);
+  const dim3 grid(tile_grid(S, kCta5), M, N);
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  if (N % KC == 0)
+    k_dequant_reduce<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, out);
+  else
+    k_dequant_reduce<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, out);
   return cudaGetLastError();
 }
 
