@@ -225,6 +225,32 @@ def test_dequant_reduce_requant_sweep_shapes(K, bits):
         check_qgz(g, block, bits, 1, K)
 
 
+# ----------------------------------------------------------------------- the sweep
+SWEEP_16M = [r for r in inputs.sweep_rows() if r["size"] == 1 << 24]
+
+
+@pytest.mark.parametrize("row", SWEEP_16M, ids=lambda r: f"{str(r['dtype'])[6:]}-int{r['bits']}-B{r['block']}-{r['kind']}")
+def test_sweep_rows_quant_dequant(row):
+    """Every sweep row (dtype x bits x block x distribution) at 2^24 elements, its own seed."""
+    x = inputs.draw(row["kind"], row["size"], seed=row["seed"], dtype=row["dtype"], device=DEV)
+    codes, scales, oc, os_ = check_quant(x, row["block"], row["bits"])
+    y = zpp.dequant_blockwise(codes, scales, x.numel(), row["block"], row["bits"], row["dtype"])
+    oy = oracle.dequant_blockwise(oc, os_, x.numel(), row["block"], row["bits"], odt(row["dtype"]))
+    assert np.array_equal(bits16(y), oy)
+
+
+@pytest.mark.parametrize("K", [2, 8, 16])
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("block", inputs.SWEEP_BLOCKS)
+def test_sweep_fused_reduction(K, bits, block):
+    """The sweep's fused dequant-reduce-requant with K in {2, 8, 16} (topology 1 x K) on
+    2^24 elements in total."""
+    n = 1 << 24
+    g = inputs.draw("laplace", n, seed=7 * K + block + bits, dtype=torch.bfloat16,
+                    device=DEV).reshape(K, n // K)
+    check_qgz(g, block, bits, 1, K)
+
+
 # ----------------------------------------------------------------------- full-size workloads
 @pytest.mark.slow
 def test_gpt_layer_full_size():
