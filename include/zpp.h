@@ -154,6 +154,20 @@ ZPP_API zpp_status zpp_dequant_reduce(const void* codes, const float* scales, in
                               int32_t block, int32_t bits, zpp_topology topo, float* out,
                               cudaStream_t stream);
 
+/*
+ * qgZ step 3 with the average folded in ([ZeRO++ abstract]: the gradient step averages
+ * the ranks' gradients). Computes the same sums as zpp_dequant_reduce, multiplies each by
+ * post_scale (one fp32 rounding; pass 1/W for the average, exact when W is a power of
+ * two) and stores the result as out_dt with round-to-nearest-even.
+ *   post_scale : finite, else ZPP_ERR_INVALID_ARG
+ *   out        : out, [W][S] elements of out_dt (ZPP_F16, ZPP_BF16 or ZPP_F32)
+ * Other arguments as in zpp_dequant_reduce.
+ */
+ZPP_API zpp_status zpp_dequant_reduce_scaled(const void* codes, const float* scales,
+                                             int64_t elems_per_rank, int32_t block, int32_t bits,
+                                             zpp_topology topo, float post_scale, void* out,
+                                             zpp_dtype out_dt, cudaStream_t stream);
+
 /* Bytes of packed codes for n elements: n for INT8, ceil(n/2) for INT4; -1 on bad bits. */
 ZPP_API int64_t zpp_code_bytes(int64_t n, int32_t bits);
 

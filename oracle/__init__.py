@@ -47,8 +47,11 @@ def lib():
         L.or_dequant_reduce_requant.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp, vp]
         L.or_dequant_reduce.argtypes = [vp, vp, i64, i64, i32, i32, i32, vp]
         L.or_qgz_passthrough.argtypes = [vp, i64, i32, i32, i32, vp]
+        L.or_dequant_reduce_scaled.argtypes = [vp, vp, i64, i64, i32, i32, i32, ctypes.c_float,
+                                               vp, i32]
         for name in ("or_quant_blockwise", "or_dequant_blockwise", "or_qgz_reorder_quant",
                      "or_dequant_reduce_requant", "or_dequant_reduce", "or_qgz_passthrough",
+                     "or_dequant_reduce_scaled",
                      "or_rounding_is_nearest"):
             getattr(L, name).restype = i32
         if not L.or_rounding_is_nearest():
@@ -178,6 +181,22 @@ def dequant_reduce(codes1, scales1, E: int, block: int, bits: int, N: int, M: in
     scales1 = _contig(scales1, np.float32).reshape(W, -1)
     out = np.zeros((W, S), np.float32)
     lib().or_dequant_reduce(_p(codes1), _p(scales1), E, block, bits, N, M, _p(out))
+    return out
+
+
+def dequant_reduce_scaled(codes1, scales1, E: int, block: int, bits: int, N: int, M: int,
+                          post_scale: float, out_dtype: int = F32):
+    """Hop 2 with the result multiplied by post_scale (1/W averages) and stored as
+    out_dtype: -> [W][S] (float32, or uint16 bits for fp16 / bf16)."""
+    W = N * M
+    _check_topo(E, block, N, M)
+    S = E // W
+    codes1 = _contig(codes1, np.uint8).reshape(W, -1)
+    scales1 = _contig(scales1, np.float32).reshape(W, -1)
+    out = np.zeros((W, S), _value_dtype(out_dtype))
+    if lib().or_dequant_reduce_scaled(_p(codes1), _p(scales1), E, block, bits, N, M,
+                                      float(post_scale), _p(out), out_dtype):
+        raise MemoryError("oracle scaled dequant-reduce failed")
     return out
 
 

@@ -350,6 +350,22 @@ int or_dequant_reduce(const uint8_t* codes1, const float* scales1, int64_t E, in
   return 0;
 }
 
+/* Step a7 with the average folded in ([ZeRO++ abstract]: the gradient step averages):
+ * the hop-2 sum of or_dequant_reduce multiplied by post_scale (one fp32 rounding; pass
+ * 1/W for the average) and stored as out_dtype with round-to-nearest-even. */
+int or_dequant_reduce_scaled(const uint8_t* codes1, const float* scales1, int64_t E,
+                             int64_t block, int bits, int N, int M, float post_scale, void* out,
+                             int out_dtype) {
+  int64_t W = (int64_t)N * M, S = E / W;
+  float* sum = (float*)malloc((size_t)(W * S) * sizeof(float));
+  if (!sum) return -1;
+  or_dequant_reduce(codes1, scales1, E, block, bits, N, M, sum);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < W * S; ++i) store_value(out, out_dtype, i, sum[i] * post_scale);
+  free(sum);
+  return 0;
+}
+
 /* The same two hops with quantisation switched off (fp32 pass-through), used to check
  * placement. reorder = 0 skips the slice reordering (the wrong layout). x [W][E] ->
  * out [W][S]. */

@@ -6,5 +6,6 @@ dequant-reduce, behind the C ABI declared in ``include/zpp.h``.
 synthetic workloads. The library is loaded on first use.
 """
 from .binding import (  # noqa: F401
-    Topology, ZppError, dequant_blockwise, dequant_reduce, dequant_reduce_requant, device_copy,
+    Topology, ZppError, dequant_blockwise, dequant_reduce, dequant_reduce_requant,
+    dequant_reduce_scaled, device_copy,
     qgz_reorder_quant, quant_blockwise, zpp_code_bytes, zpp_num_scales, zpp_status_string)

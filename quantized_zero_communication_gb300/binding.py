@@ -51,6 +51,8 @@ def lib():
         "zpp_qgz_reorder_quant": [vp, i32, i64, i32, i32, Topology, vp, vp, vp],
         "zpp_dequant_reduce_requant": [vp, vp, i64, i32, i32, Topology, vp, vp, vp],
         "zpp_dequant_reduce": [vp, vp, i64, i32, i32, Topology, vp, vp],
+        "zpp_dequant_reduce_scaled": [vp, vp, i64, i32, i32, Topology, ctypes.c_float, vp, i32,
+                                      vp],
         "zpp_device_copy": [vp, vp, i64, vp],
     }
     for name, args in sig.items():
@@ -95,6 +97,12 @@ def zpp_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits, topo,
 
 def zpp_dequant_reduce(codes, scales, elems_per_rank, block, bits, topo, out, stream=0):
     return lib().zpp_dequant_reduce(codes, scales, elems_per_rank, block, bits, topo, out, stream)
+
+
+def zpp_dequant_reduce_scaled(codes, scales, elems_per_rank, block, bits, topo, post_scale, out,
+                              out_dt, stream=0):
+    return lib().zpp_dequant_reduce_scaled(codes, scales, elems_per_rank, block, bits, topo,
+                                           post_scale, out, out_dt, stream)
 
 
 def zpp_device_copy(src, dst, nbytes, stream=0):
@@ -207,6 +215,23 @@ def dequant_reduce(codes, scales, E, block, bits, N, M, out=None):
         out = torch.empty((W, E // W), dtype=torch.float32, device=codes.device)
     _check(zpp_dequant_reduce(codes.data_ptr(), scales.data_ptr(), E, block, bits, Topology(N, M),
                               out.data_ptr(), _stream(codes)), "zpp_dequant_reduce")
+    return out
+
+
+def dequant_reduce_scaled(codes, scales, E, block, bits, N, M, post_scale=None, dtype=None,
+                          out=None):
+    """Inter-node hop with the average folded in: [W][E/W] of `dtype` (default fp32) holding
+    fp32(sum * post_scale); post_scale defaults to 1/W (the average over ranks)."""
+    torch = _torch()
+    _cuda(codes, scales)
+    W = N * M
+    if post_scale is None:
+        post_scale = 1.0 / W
+    if out is None:
+        out = torch.empty((W, E // W), dtype=dtype or torch.float32, device=codes.device)
+    _check(zpp_dequant_reduce_scaled(codes.data_ptr(), scales.data_ptr(), E, block, bits,
+                                     Topology(N, M), float(post_scale), out.data_ptr(),
+                                     _dt(out.dtype), _stream(codes)), "zpp_dequant_reduce_scaled")
     return out
 
 

@@ -16,10 +16,6 @@
 
 namespace zpp {
 
-struct OutF16 {};
-struct OutBF16 {};
-struct OutF32 {};
-
 constexpr int kDqVec = 16;                 // elements per lane per row
 constexpr int kDqRow = 32 * kDqVec;        // 512
 constexpr int kDqRows = 4;
@@ -56,27 +52,6 @@ __device__ __forceinline__ void dequant16(const uint32_t w[4], float s, float v[
 #pragma unroll
       for (int j = 0; j < 4; ++j) f2_split(f2_mul(q[j], ss), v[8 * k + 2 * j], v[8 * k + 2 * j + 1]);
     }
-  }
-}
-
-template <typename OT>
-__device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
-  if constexpr (std::is_same_v<OT, OutF32>) {
-    U8x32 a, b;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      a.w[i] = __float_as_uint(v[i]);
-      b.w[i] = __float_as_uint(v[8 + i]);
-    }
-    float* p = static_cast<float*>(y) + e;
-    st_v8(p, a);
-    st_v8(p + 8, b);
-  } else {
-    using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
-    U8x32 a;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
-    st_v8(static_cast<uint16_t*>(y) + e, a);
   }
 }
 

@@ -164,11 +164,13 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
-// slice and writes them as two 256-bit stores (each a full 32-byte sector).
-template <int BITS, int KC, bool EXACT>
+// slice: the sums, multiplied by post_scale (1 for the plain sum, 1/W for the average; one
+// fp32 rounding), are written with 256-bit stores as fp32 (each store a full 32-byte
+// sector) or rounded to fp16 / bf16.
+template <int BITS, int KC, bool EXACT, typename OT>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t E,
-                     int log2b, int N, int M, float* __restrict__ out) {
+                     int log2b, int N, int M, float post_scale, void* __restrict__ out) {
   constexpr int NW = BITS == 8 ? 4 : 2;  // code words per lane per source
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = blockIdx.y, n = blockIdx.z;
@@ -187,18 +189,11 @@ __global__ void __launch_bounds__(kThreads)
   for (int j = 0; j < 8; ++j) acc[j] = f2(0.0f, 0.0f);
   reduce_sources<BITS, NW, KC, EXACT>(acc, cbase, static_cast<int64_t>(M) * cb, sbase,
                                       static_cast<int64_t>(M) * sc, N, true);
-  U8x32 a, b;
+  const f32x2 ps = f2(post_scale, post_scale);
+  float v[16];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float lo, hi;
-    f2_split(acc[j], lo, hi);
-    a.w[2 * j] = __float_as_uint(lo), a.w[2 * j + 1] = __float_as_uint(hi);
-    f2_split(acc[4 + j], lo, hi);
-    b.w[2 * j] = __float_as_uint(lo), b.w[2 * j + 1] = __float_as_uint(hi);
-  }
-  float* p = out + r * S + e;
-  st_v8(p, a);
-  st_v8(p + 8, b);
+  for (int j = 0; j < 8; ++j) f2_split(f2_mul(acc[j], ps), v[2 * j], v[2 * j + 1]);
+  store16<OT>(out, r * S + e, v);
 }
 
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
@@ -216,16 +211,18 @@ static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, in
   return cudaGetLastError();
 }
 
-template <int BITS, int KC>
+template <int BITS, int KC, typename OT>
 static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                          int M, float* out, cudaStream_t s) {
+                          int M, float post_scale, void* out, cudaStream_t s) {
   const int64_t S = E / (static_cast<int64_t>(N) * M);
   const dim3 grid(tile_grid(S, kCta5), M, N);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   if (N % KC == 0)
-    k_dequant_reduce<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, out);
+    k_dequant_reduce<BITS, KC, true, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
+                                                                   post_scale, out);
   else
-    k_dequant_reduce<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, out);
+    k_dequant_reduce<BITS, KC, false, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
+                                                                    post_scale, out);
   return cudaGetLastError();
 }
 
@@ -240,15 +237,22 @@ static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int log2b
   }
 }
 
-template <int BITS>
+template <int BITS, typename OT>
 static cudaError_t dr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
-                           float* out, cudaStream_t s) {
+                           float ps, void* out, cudaStream_t s) {
   switch (chunk_for(N)) {
-    case 8: return run_dr<BITS, 8>(c, sc, E, log2b, N, M, out, s);
-    case 4: return run_dr<BITS, 4>(c, sc, E, log2b, N, M, out, s);
-    case 2: return run_dr<BITS, 2>(c, sc, E, log2b, N, M, out, s);
-    default: return run_dr<BITS, 1>(c, sc, E, log2b, N, M, out, s);
+    case 8: return run_dr<BITS, 8, OT>(c, sc, E, log2b, N, M, ps, out, s);
+    case 4: return run_dr<BITS, 4, OT>(c, sc, E, log2b, N, M, ps, out, s);
+    case 2: return run_dr<BITS, 2, OT>(c, sc, E, log2b, N, M, ps, out, s);
+    default: return run_dr<BITS, 1, OT>(c, sc, E, log2b, N, M, ps, out, s);
   }
+}
+
+template <typename OT>
+static cudaError_t dr_out(const void* c, const float* sc, int64_t E, int log2b, int bits, int N,
+                          int M, float ps, void* out, cudaStream_t s) {
+  return bits == 8 ? dr_bits<8, OT>(c, sc, E, log2b, N, M, ps, out, s)
+                   : dr_bits<4, OT>(c, sc, E, log2b, N, M, ps, out, s);
 }
 
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
@@ -260,10 +264,12 @@ cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales
 }
 
 cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, float* out, cudaStream_t s) {
+                                  int bits, int N, int M, float post_scale, void* out, int out_kind,
+                                  cudaStream_t s) {
   const int log2b = __builtin_ctz(static_cast<unsigned>(block));
-  return bits == 8 ? dr_bits<8>(codes, scales, E, log2b, N, M, out, s)
-                   : dr_bits<4>(codes, scales, E, log2b, N, M, out, s);
+  if (out_kind == 0) return dr_out<OutF16>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
+  if (out_kind == 1) return dr_out<OutBF16>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
+  return dr_out<OutF32>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
 }
 
 }  // namespace zpp

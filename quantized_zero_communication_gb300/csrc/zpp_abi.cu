@@ -146,7 +146,25 @@ zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t el
   if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
   if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
-                                              topo.num_nodes, topo.gpus_per_node, out, stream));
+                                              topo.num_nodes, topo.gpus_per_node, 1.0f, out,
+                                              ZPP_F32, stream));
+}
+
+zpp_status zpp_dequant_reduce_scaled(const void* codes, const float* scales,
+                                     int64_t elems_per_rank, int32_t block, int32_t bits,
+                                     zpp_topology topo, float post_scale, void* out,
+                                     zpp_dtype out_dt, cudaStream_t stream) {
+  int64_t W = 0;
+  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (out_dt != ZPP_F16 && out_dt != ZPP_BF16 && out_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (!(post_scale == post_scale) || post_scale - post_scale != 0.0f) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0) return ZPP_OK;
+  if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
+                                              topo.num_nodes, topo.gpus_per_node, post_scale, out,
+                                              static_cast<int>(out_dt), stream));
 }
 
 zpp_status zpp_device_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream) {

@@ -12,6 +12,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace zpp {
 
 constexpr int kThreads = 256;  // threads per CTA for every kernel (8 warps)
@@ -245,6 +247,34 @@ __device__ __forceinline__ uint32_t pack_int8x4(const f32x2 r[2]) {
 // |x * inv| <= qmax (1 + 2^-24), which rounds to at most qmax.
 __device__ __forceinline__ f32x2 round_codes(f32x2 x, f32x2 inv2) {
   return f2_fma(x, inv2, f2(kRoundMagic, kRoundMagic));
+}
+
+// Output element types of the dequantising kernels.
+struct OutF16 {};
+struct OutBF16 {};
+struct OutF32 {};
+
+// 16 consecutive fp32 values -> y[e .. e+16) of type OT (fp32: two 256-bit stores;
+// fp16 / bf16: round to nearest even, one 256-bit store).
+template <typename OT>
+__device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
+  if constexpr (std::is_same_v<OT, OutF32>) {
+    U8x32 a, b;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a.w[i] = __float_as_uint(v[i]);
+      b.w[i] = __float_as_uint(v[8 + i]);
+    }
+    float* p = static_cast<float*>(y) + e;
+    st_v8(p, a);
+    st_v8(p + 8, b);
+  } else {
+    using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
+    U8x32 a;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
+    st_v8(static_cast<uint16_t*>(y) + e, a);
+  }
 }
 
 __device__ __forceinline__ float warp_max(float v, int width) {

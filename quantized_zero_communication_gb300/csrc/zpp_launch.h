@@ -25,9 +25,11 @@ cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales
                                           int block, int bits, int N, int M, void* out_codes,
                                           float* out_scales, cudaStream_t s);
 
-// K5: inter-node dequantise -> fp32 sum over N slices.
+// K5: inter-node dequantise -> fp32 sum over N slices, times post_scale, stored as fp16
+// (out_kind 0), bf16 (1) or fp32 (2).
 cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, float* out, cudaStream_t s);
+                                  int bits, int N, int M, float post_scale, void* out, int out_kind,
+                                  cudaStream_t s);
 
 // K6: 256-bit device copy (the same-run HBM reference).
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s);

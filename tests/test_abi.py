@@ -18,7 +18,7 @@ FAKE = 0x10000  # 64 KiB: 32-byte aligned, never dereferenced
 def test_library_exports_every_declared_symbol():
     names = zb.declared_symbols()
     assert {"zpp_quant_blockwise", "zpp_dequant_blockwise", "zpp_qgz_reorder_quant",
-            "zpp_dequant_reduce_requant", "zpp_dequant_reduce"} <= set(names)
+            "zpp_dequant_reduce_requant", "zpp_dequant_reduce", "zpp_dequant_reduce_scaled"} <= set(names)
     L = zb.lib()
     for name in names:
         assert hasattr(L, name), name
@@ -110,6 +110,13 @@ def test_qgz_entry_points_reject_bad_topologies():
         assert f(8 * 128, 128, 4, T(2, 4), FAKE + 16) == zb.ZPP_ERR_MISALIGNED
     assert zb.zpp_qgz_reorder_quant(FAKE, zb.ZPP_F32, 1024, 128, 4, T(2, 4), FAKE,
                                     FAKE) == zb.ZPP_ERR_UNSUPPORTED
+    sc = zb.zpp_dequant_reduce_scaled
+    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE, 5) == zb.ZPP_ERR_INVALID_ARG
+    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), float("nan"), FAKE, 2) == zb.ZPP_ERR_INVALID_ARG
+    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), float("inf"), FAKE, 2) == zb.ZPP_ERR_INVALID_ARG
+    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE + 16, 1) == zb.ZPP_ERR_MISALIGNED
+    assert sc(FAKE, FAKE, 1000, 128, 4, T(2, 4), 0.125, FAKE, 1) == zb.ZPP_ERR_INVALID_ARG
+    assert sc(FAKE, FAKE, 0, 128, 4, T(2, 4), 0.125, FAKE, 1) == zb.ZPP_OK
 
 
 @cpu_only

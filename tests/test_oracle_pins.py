@@ -409,3 +409,45 @@ def test_golden_qgz_fused_sum():
     dt = oracle.F16 if case["dtype"] == "f16" else oracle.BF16
     res = oracle.qgz_pipeline(bits16(g), dt, case["block"], case["bits"], case["N"], case["M"])
     check_qgz_case(case, *res)
+
+
+@pytest.mark.parametrize("N,M", [(2, 2), (2, 4), (1, 8)])
+def test_average_of_identical_exact_sources_is_the_own_slice(N, M):
+    """The abstract describes the gradient step as an average: with every rank holding the
+    same exactly representable gradient, the averaged owner slice (post_scale 1/W, W a power
+    of two) is the rank's own slice, exactly, in fp32 and after the bf16 cast."""
+    W, B, bits = N * M, 64, 4
+    qmax = 7
+    S = 2 * B
+    E = W * S
+    rng = np.random.default_rng(100 + W)
+    nblk = E // B
+    k = rng.integers(-qmax, qmax + 1, (nblk, B))
+    k[np.arange(nblk), rng.integers(0, B, nblk)] = -qmax
+    e = rng.integers(-6, 2, nblk)[:, None]
+    row = (k * np.exp2(e.astype(np.float64))).reshape(-1)
+    g = torch.from_numpy(np.tile(row, (W, 1))).to(torch.bfloat16)
+    c0, s0, c1, s1, _ = oracle.qgz_pipeline(bits16(g), oracle.BF16, B, bits, N, M)
+    avg = oracle.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, 1.0 / W, oracle.F32)
+    assert np.array_equal(avg, row.astype(np.float32).reshape(W, S))
+    avg16 = oracle.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, 1.0 / W, oracle.BF16)
+    assert np.array_equal(avg16, bits16(torch.from_numpy(row).to(torch.bfloat16)).reshape(W, S))
+
+
+def test_averaged_two_hop_result_within_bound():
+    """The averaged (1/W) owner slices of the 2 x 4 workload stay within the two-quantisation
+    bound of the direct average, in fp32 and after a bf16 cast (plus half a bf16 ulp)."""
+    N, M, B, bits = 2, 4, 128, 4
+    g = inputs.qgz_tiny()
+    W, E = g.shape
+    S = E // W
+    xs = g.double().numpy()
+    c0, s0, c1, s1, total = oracle.qgz_pipeline(bits16(g), oracle.BF16, B, bits, N, M)
+    direct = np.stack([xs[:, r * S:(r + 1) * S].sum(0) for r in range(W)]) / W
+    bound = _two_hop_bound(xs, N, M, B, bits) / W
+    avg = oracle.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, 1.0 / W, oracle.F32).astype(np.float64)
+    assert np.all(np.abs(avg - direct) <= bound + U * np.abs(avg))
+    a16 = f32_of_bits(oracle.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, 1.0 / W, oracle.BF16),
+                      oracle.BF16).astype(np.float64)
+    half_ulp = np.abs(a16) * 2.0 ** -8
+    assert np.all(np.abs(a16 - direct) <= bound + U * np.abs(avg) + half_ulp)

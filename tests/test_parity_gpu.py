@@ -196,6 +196,30 @@ def test_qgz_pipeline_topologies(N, M, bits):
             check_qgz(g, block, bits, N, M)
 
 
+@pytest.mark.parametrize("N,M", [(2, 4), (3, 2), (4, 8)])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_averaged_owner_slices(N, M, bits):
+    """zpp_dequant_reduce_scaled: 1/W (and an arbitrary scale) into fp32, bf16 and fp16."""
+    W, B = N * M, 256
+    E = W * 2 * 4096
+    g = inputs.draw("laplace", W * E, seed=W * bits, dtype=torch.bfloat16, device=DEV).reshape(W, E)
+    c0, s0 = zpp.qgz_reorder_quant(g, B, bits, N, M)
+    c1, s1 = zpp.dequant_reduce_requant(c0, s0, E, B, bits, N, M)
+    oc1, os1 = host(c1), host(s1)
+    plain = zpp.dequant_reduce(c1, s1, E, B, bits, N, M)
+    for ps in (1.0 / W, 0.3, 1.0):
+        for dt in (torch.float32, torch.bfloat16, torch.float16):
+            got = zpp.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, post_scale=ps, dtype=dt)
+            want = oracle.dequant_reduce_scaled(oc1, os1, E, B, bits, N, M, ps, odt(dt))
+            if dt == torch.float32:
+                assert_f32_parity(host(got), want)
+            else:
+                assert np.array_equal(bits16(got), want)
+    one = zpp.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, post_scale=1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(one, plain)
+
+
 def test_qgz_fp16_gradients():
     g = inputs.draw("normal", 8 * 8 * 1024, seed=4, dtype=torch.float16, device=DEV).reshape(8, -1)
     check_qgz(g, 128, 4, 2, 4)
