@@ -319,6 +319,8 @@ def run_ours(args):
             "traffic": ncu_traffic(dom, per_kernel_bytes[dom] / full_bytes)}
     # same-run copy kernel on 1 GiB (reference for the same HBM)
     copy_gbs = None if args.only else _copy_reference(zpp, torch, dev)
+    overlap = None if args.only else _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out,
+                                                  per_kernel_bytes)
 
     result = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -328,6 +330,7 @@ def run_ours(args):
               "config": workload_config(div, n_qwz, E),
               "roofline": roof, "kernels": kernels,
               "copy_kernel_gbs": round(copy_gbs, 1) if copy_gbs else None,
+              "qgz_pipelined": overlap,
               "gpu_launches": len(active) * args.steps, "clocks": clocks}
     if args.only:
         result["only"] = active[0]
@@ -369,6 +372,50 @@ def _copy_reference(zpp, torch, dev):
     t = s.elapsed_time(e) / 10 * 1e-3
     del a, b
     return 2 * (1 << 30) / t / 1e9
+
+
+def _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out, per_kernel_bytes, reps=20):
+    """The qgZ half (K3 -> K4 -> K5) timed as three whole-exchange launches and as M
+    independent local-index sub-pipelines spread over side streams, where one chunk's
+    ALU-bound fused hop overlaps another chunk's memory-bound reorder+quantise."""
+    N, M = QGZ_N, QGZ_M
+    stream = torch.cuda.current_stream(dev)
+    bufs = zpp.QgzBuffers.__new__(zpp.QgzBuffers)
+    bufs.c0, bufs.s0, bufs.c1, bufs.s1, bufs.out = c0, s0, c1, s1, out
+    qbytes = sum(per_kernel_bytes[k] for k in KERNELS[2:])
+
+    def serial():
+        zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
+        zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
+        zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    res = {"serial_us": round(timed(serial), 1)}
+    for n_streams in (2, 4):
+        streams = [torch.cuda.Stream(dev) for _ in range(n_streams)]
+        us = timed(lambda: zpp.qgz_pipelined(g, QGZ_BLOCK, QGZ_BITS, N, M, bufs=bufs,
+                                             streams=streams))
+        res[f"pipelined_{n_streams}_streams_us"] = round(us, 1)
+    lo, hi = torch.cuda.Stream(dev, priority=0), torch.cuda.Stream(dev, priority=-1)
+    for chunks in (1, 2):
+        us = timed(lambda: zpp.qgz_pipelined(g, QGZ_BLOCK, QGZ_BITS, N, M, bufs=bufs,
+                                             streams=("split", lo, hi), chunks=chunks))
+        res[f"pipelined_split_priority_{chunks}_chunk_us"] = round(us, 1)
+    best = min(v for k, v in res.items() if k.startswith("pipelined"))
+    res["gbs_serial"] = round(qbytes / (res["serial_us"] * 1e-6) / 1e9, 1)
+    res["gbs_pipelined"] = round(qbytes / (best * 1e-6) / 1e9, 1)
+    return res
 
 
 def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, n_qwz, E,

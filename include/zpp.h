@@ -75,6 +75,17 @@ typedef struct zpp_topology {
   int32_t gpus_per_node; /* M >= 1 */
 } zpp_topology;
 
+/* A range [begin, end) of local GPU indices l (0 <= begin <= end <= M). The qgZ exchange
+ * splits exactly by l: hop-1 chunk l of every rank feeds only the receivers with local
+ * index l, whose hop-1 outputs feed only the hop-2 receivers with local index l. So the
+ * three qgZ steps restricted to one range form an independent sub-pipeline, and the
+ * ranges of a partition of [0, M) may run on different streams (the pipelining of the
+ * intra- and inter-node hops, on one GPU). */
+typedef struct zpp_local_range {
+  int32_t begin;
+  int32_t end;
+} zpp_local_range;
+
 /* Limits checked by every entry point. */
 #define ZPP_MIN_BLOCK 64
 #define ZPP_MAX_BLOCK 4096
@@ -167,6 +178,33 @@ ZPP_API zpp_status zpp_dequant_reduce_scaled(const void* codes, const float* sca
                                              int64_t elems_per_rank, int32_t block, int32_t bits,
                                              zpp_topology topo, float post_scale, void* out,
                                              zpp_dtype out_dt, cudaStream_t stream);
+
+/*
+ * The three qgZ steps restricted to the local indices of `range` ([ZeRO++ summary]
+ * Approach: overlapped intra- and inter-node pipelining). Buffers have the full layouts
+ * of the unrestricted calls; only the parts that belong to the range are read or written:
+ *   zpp_qgz_reorder_quant_range     writes chunks l in range of every rank's codes/scales
+ *   zpp_dequant_reduce_requant_range writes the hop-1 output of receivers (n, l), l in range
+ *   zpp_dequant_reduce_scaled_range  writes the owner slices of ranks (n, l), l in range
+ * An empty range returns ZPP_OK and launches nothing; a range outside [0, M] is
+ * ZPP_ERR_INVALID_ARG. Results are bit-identical to the unrestricted calls.
+ */
+ZPP_API zpp_status zpp_qgz_reorder_quant_range(const void* grads, zpp_dtype g_dt,
+                                               int64_t elems_per_rank, int32_t block,
+                                               int32_t bits, zpp_topology topo,
+                                               zpp_local_range range, void* codes,
+                                               float* scales, cudaStream_t stream);
+ZPP_API zpp_status zpp_dequant_reduce_requant_range(const void* codes, const float* scales,
+                                                    int64_t elems_per_rank, int32_t block,
+                                                    int32_t bits, zpp_topology topo,
+                                                    zpp_local_range range, void* out_codes,
+                                                    float* out_scales, cudaStream_t stream);
+ZPP_API zpp_status zpp_dequant_reduce_scaled_range(const void* codes, const float* scales,
+                                                   int64_t elems_per_rank, int32_t block,
+                                                   int32_t bits, zpp_topology topo,
+                                                   zpp_local_range range, float post_scale,
+                                                   void* out, zpp_dtype out_dt,
+                                                   cudaStream_t stream);
 
 /* Bytes of packed codes for n elements: n for INT8, ceil(n/2) for INT4; -1 on bad bits. */
 ZPP_API int64_t zpp_code_bytes(int64_t n, int32_t bits);

@@ -22,6 +22,10 @@ class Topology(ctypes.Structure):
     _fields_ = [("num_nodes", ctypes.c_int32), ("gpus_per_node", ctypes.c_int32)]
 
 
+class LocalRange(ctypes.Structure):
+    _fields_ = [("begin", ctypes.c_int32), ("end", ctypes.c_int32)]
+
+
 class ZppError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -53,6 +57,11 @@ def lib():
         "zpp_dequant_reduce": [vp, vp, i64, i32, i32, Topology, vp, vp],
         "zpp_dequant_reduce_scaled": [vp, vp, i64, i32, i32, Topology, ctypes.c_float, vp, i32,
                                       vp],
+        "zpp_qgz_reorder_quant_range": [vp, i32, i64, i32, i32, Topology, LocalRange, vp, vp, vp],
+        "zpp_dequant_reduce_requant_range": [vp, vp, i64, i32, i32, Topology, LocalRange, vp, vp,
+                                             vp],
+        "zpp_dequant_reduce_scaled_range": [vp, vp, i64, i32, i32, Topology, LocalRange,
+                                            ctypes.c_float, vp, i32, vp],
         "zpp_device_copy": [vp, vp, i64, vp],
     }
     for name, args in sig.items():
@@ -103,6 +112,24 @@ def zpp_dequant_reduce_scaled(codes, scales, elems_per_rank, block, bits, topo, 
                               out_dt, stream=0):
     return lib().zpp_dequant_reduce_scaled(codes, scales, elems_per_rank, block, bits, topo,
                                            post_scale, out, out_dt, stream)
+
+
+def zpp_qgz_reorder_quant_range(grads, g_dt, elems_per_rank, block, bits, topo, rng, codes,
+                                scales, stream=0):
+    return lib().zpp_qgz_reorder_quant_range(grads, g_dt, elems_per_rank, block, bits, topo, rng,
+                                             codes, scales, stream)
+
+
+def zpp_dequant_reduce_requant_range(codes, scales, elems_per_rank, block, bits, topo, rng,
+                                     out_codes, out_scales, stream=0):
+    return lib().zpp_dequant_reduce_requant_range(codes, scales, elems_per_rank, block, bits,
+                                                  topo, rng, out_codes, out_scales, stream)
+
+
+def zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, topo, rng,
+                                    post_scale, out, out_dt, stream=0):
+    return lib().zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits,
+                                                 topo, rng, post_scale, out, out_dt, stream)
 
 
 def zpp_device_copy(src, dst, nbytes, stream=0):
@@ -233,6 +260,75 @@ def dequant_reduce_scaled(codes, scales, E, block, bits, N, M, post_scale=None, 
                                      Topology(N, M), float(post_scale), out.data_ptr(),
                                      _dt(out.dtype), _stream(codes)), "zpp_dequant_reduce_scaled")
     return out
+
+
+class QgzBuffers:
+    """Device buffers of one qgZ exchange: reordered codes/scales, hop-1 codes/scales and
+    the owner slices."""
+
+    def __init__(self, W, E, block, bits, M, device, out_dtype=None):
+        torch = _torch()
+        C = E // M
+        self.c0 = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=device)
+        self.s0 = torch.empty((W, E // block), dtype=torch.float32, device=device)
+        self.c1 = torch.empty((W, zpp_code_bytes(C, bits)), dtype=torch.uint8, device=device)
+        self.s1 = torch.empty((W, C // block), dtype=torch.float32, device=device)
+        self.out = torch.empty((W, E // W), dtype=out_dtype or torch.float32, device=device)
+
+
+def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=None,
+                  n_streams=2, chunks=None):
+    """The whole qgZ exchange as independent local-index sub-pipelines (reorder + quantise
+    of chunks l, hop 1 for receivers (n, l), hop 2 for ranks (n, l)), joined back into the
+    caller's stream. `chunks` local indices form one sub-pipeline (default: one per l).
+
+    Schedules: with a list of `streams`, whole sub-pipelines go round robin over them;
+    with ``streams=("split", low, high)`` every reorder + quantise runs on the `low`
+    stream and each sub-pipeline's two hops on the `high` stream, gated by an event, so
+    hop work fills the SMs that reorder work frees (give `high` the higher priority).
+    Returns the buffers (owner slices in ``bufs.out``; fp32 by default)."""
+    torch = _torch()
+    _cuda(grads)
+    W = N * M
+    E = grads.numel() // W
+    if bufs is None:
+        bufs = QgzBuffers(W, E, block, bits, M, grads.device)
+    main = torch.cuda.current_stream(grads.device)
+    if streams is None:
+        streams = [torch.cuda.Stream(grads.device) for _ in range(min(n_streams, M))]
+    split = len(streams) == 3 and streams[0] == "split"
+    side = list(streams[1:]) if split else list(streams)
+    chunks = chunks or 1
+    fork = torch.cuda.Event()
+    fork.record(main)
+    topo = Topology(N, M)
+    gdt, odt = _dt(grads.dtype), _dt(bufs.out.dtype)
+    for st in side:
+        st.wait_event(fork)
+    for i, l0 in enumerate(range(0, M, chunks)):
+        rng = LocalRange(l0, min(M, l0 + chunks))
+        st_q = side[0] if split else side[i % len(side)]
+        st_h = side[1] if split else st_q
+        _check(zpp_qgz_reorder_quant_range(grads.data_ptr(), gdt, E, block, bits, topo, rng,
+                                           bufs.c0.data_ptr(), bufs.s0.data_ptr(),
+                                           st_q.cuda_stream), "zpp_qgz_reorder_quant_range")
+        if split:
+            ready = torch.cuda.Event()
+            ready.record(st_q)
+            st_h.wait_event(ready)
+        _check(zpp_dequant_reduce_requant_range(bufs.c0.data_ptr(), bufs.s0.data_ptr(), E, block,
+                                                bits, topo, rng, bufs.c1.data_ptr(),
+                                                bufs.s1.data_ptr(), st_h.cuda_stream),
+               "zpp_dequant_reduce_requant_range")
+        _check(zpp_dequant_reduce_scaled_range(bufs.c1.data_ptr(), bufs.s1.data_ptr(), E, block,
+                                               bits, topo, rng, float(post_scale),
+                                               bufs.out.data_ptr(), odt, st_h.cuda_stream),
+               "zpp_dequant_reduce_scaled_range")
+    for st in side:
+        join = torch.cuda.Event()
+        join.record(st)
+        main.wait_event(join)
+    return bufs
 
 
 def device_copy(src, dst):

@@ -86,18 +86,19 @@ __device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase,
   }
 }
 
-// K4. Grid (tile, l, n): CTA (x, l, n) owns tile x of receiver (n, l) -- 8 warps x one row
-// each -- so no thread divides to find its work. Blocks wider than a row are reduced
+// K4. Grid (tile, l - l_begin, n): CTA (x, l, n) owns tile x of receiver (n, l) -- 8 warps
+// x one row each -- so no thread divides to find its work. A launch may cover only the
+// receivers whose local index l lies in [l_begin, l_begin + gridDim.y). Blocks wider than a row are reduced
 // across the warps that share them through shared memory.
 template <int BITS, int KC, bool EXACT, bool FULL>
 __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
                                          const float* __restrict__ scales, int64_t E, int log2b,
-                                         int M, uint8_t* __restrict__ out_codes,
+                                         int M, int l_begin, uint8_t* __restrict__ out_codes,
                                          float* __restrict__ out_scales, float* red) {
   using G = Geo4<BITS>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int B = 1 << log2b;
-  const int l = blockIdx.y, n = blockIdx.z;
+  const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
   const int64_t C = E / M;  // = N * S, the hop-1 chunk
   const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
@@ -153,14 +154,14 @@ __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
 template <int BITS, int KC, bool EXACT>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce_requant(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
-                             int64_t E, int log2b, int M, uint8_t* __restrict__ out_codes,
-                             float* __restrict__ out_scales) {
+                             int64_t E, int log2b, int M, int l_begin,
+                             uint8_t* __restrict__ out_codes, float* __restrict__ out_scales) {
   __shared__ float red[kWarps];
   const int64_t C = E / M;
   if ((static_cast<int64_t>(blockIdx.x) + 1) * Geo4<BITS>::CTA <= C)  // CTA-uniform
-    drr_tile<BITS, KC, EXACT, true>(codes, scales, E, log2b, M, out_codes, out_scales, red);
+    drr_tile<BITS, KC, EXACT, true>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales, red);
   else
-    drr_tile<BITS, KC, EXACT, false>(codes, scales, E, log2b, M, out_codes, out_scales, red);
+    drr_tile<BITS, KC, EXACT, false>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales, red);
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
@@ -170,10 +171,10 @@ __global__ void __launch_bounds__(kThreads)
 template <int BITS, int KC, bool EXACT, typename OT>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t E,
-                     int log2b, int N, int M, float post_scale, void* __restrict__ out) {
+                     int log2b, int N, int M, int l_begin, float post_scale, void* __restrict__ out) {
   constexpr int NW = BITS == 8 ? 4 : 2;  // code words per lane per source
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int l = blockIdx.y, n = blockIdx.z;
+  const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
   const int64_t W = static_cast<int64_t>(N) * M;
   const int64_t S = E / W, C = E / M;
@@ -200,76 +201,84 @@ static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1))
 
 template <int BITS, int KC>
 static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                           int M, void* out_codes, float* out_scales, cudaStream_t s) {
-  const dim3 grid(tile_grid(E / M, Geo4<BITS>::CTA), M, N);
+                           int M, int lb, int le, void* out_codes, float* out_scales,
+                           cudaStream_t s) {
+  const dim3 grid(tile_grid(E / M, Geo4<BITS>::CTA), le - lb, N);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
   if (M % KC == 0)
-    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, oc, out_scales);
+    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, oc,
+                                                                       out_scales);
   else
-    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, oc, out_scales);
+    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, oc,
+                                                                        out_scales);
   return cudaGetLastError();
 }
 
 template <int BITS, int KC, typename OT>
 static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                          int M, float post_scale, void* out, cudaStream_t s) {
+                          int M, int lb, int le, float post_scale, void* out, cudaStream_t s) {
   const int64_t S = E / (static_cast<int64_t>(N) * M);
-  const dim3 grid(tile_grid(S, kCta5), M, N);
+  const dim3 grid(tile_grid(S, kCta5), le - lb, N);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   if (N % KC == 0)
-    k_dequant_reduce<BITS, KC, true, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
+    k_dequant_reduce<BITS, KC, true, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, lb,
                                                                    post_scale, out);
   else
-    k_dequant_reduce<BITS, KC, false, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
+    k_dequant_reduce<BITS, KC, false, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, lb,
                                                                     post_scale, out);
   return cudaGetLastError();
 }
 
 template <int BITS>
 static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
-                            void* oc, float* os, cudaStream_t s) {
+                            int lb, int le, void* oc, float* os, cudaStream_t s) {
   switch (chunk_for(M)) {
-    case 8: return run_drr<BITS, 8>(c, sc, E, log2b, N, M, oc, os, s);
-    case 4: return run_drr<BITS, 4>(c, sc, E, log2b, N, M, oc, os, s);
-    case 2: return run_drr<BITS, 2>(c, sc, E, log2b, N, M, oc, os, s);
-    default: return run_drr<BITS, 1>(c, sc, E, log2b, N, M, oc, os, s);
+    case 8: return run_drr<BITS, 8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    case 4: return run_drr<BITS, 4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    case 2: return run_drr<BITS, 2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    default: return run_drr<BITS, 1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
   }
 }
 
 template <int BITS, typename OT>
 static cudaError_t dr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
-                           float ps, void* out, cudaStream_t s) {
+                           int lb, int le, float ps, void* out, cudaStream_t s) {
   switch (chunk_for(N)) {
-    case 8: return run_dr<BITS, 8, OT>(c, sc, E, log2b, N, M, ps, out, s);
-    case 4: return run_dr<BITS, 4, OT>(c, sc, E, log2b, N, M, ps, out, s);
-    case 2: return run_dr<BITS, 2, OT>(c, sc, E, log2b, N, M, ps, out, s);
-    default: return run_dr<BITS, 1, OT>(c, sc, E, log2b, N, M, ps, out, s);
+    case 8: return run_dr<BITS, 8, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
+    case 4: return run_dr<BITS, 4, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
+    case 2: return run_dr<BITS, 2, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
+    default: return run_dr<BITS, 1, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
   }
 }
 
 template <typename OT>
 static cudaError_t dr_out(const void* c, const float* sc, int64_t E, int log2b, int bits, int N,
-                          int M, float ps, void* out, cudaStream_t s) {
-  return bits == 8 ? dr_bits<8, OT>(c, sc, E, log2b, N, M, ps, out, s)
-                   : dr_bits<4, OT>(c, sc, E, log2b, N, M, ps, out, s);
+                          int M, int lb, int le, float ps, void* out, cudaStream_t s) {
+  return bits == 8 ? dr_bits<8, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s)
+                   : dr_bits<4, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
 }
 
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
-                                          int block, int bits, int N, int M, void* out_codes,
-                                          float* out_scales, cudaStream_t s) {
+                                          int block, int bits, int N, int M, int l_begin,
+                                          int l_end, void* out_codes, float* out_scales,
+                                          cudaStream_t s) {
   const int log2b = __builtin_ctz(static_cast<unsigned>(block));
-  return bits == 8 ? drr_bits<8>(codes, scales, E, log2b, N, M, out_codes, out_scales, s)
-                   : drr_bits<4>(codes, scales, E, log2b, N, M, out_codes, out_scales, s);
+  return bits == 8 ? drr_bits<8>(codes, scales, E, log2b, N, M, l_begin, l_end, out_codes,
+                                 out_scales, s)
+                   : drr_bits<4>(codes, scales, E, log2b, N, M, l_begin, l_end, out_codes,
+                                 out_scales, s);
 }
 
 cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, float post_scale, void* out, int out_kind,
-                                  cudaStream_t s) {
+                                  int bits, int N, int M, int l_begin, int l_end, float post_scale,
+                                  void* out, int out_kind, cudaStream_t s) {
   const int log2b = __builtin_ctz(static_cast<unsigned>(block));
-  if (out_kind == 0) return dr_out<OutF16>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
-  if (out_kind == 1) return dr_out<OutBF16>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
-  return dr_out<OutF32>(codes, scales, E, log2b, bits, N, M, post_scale, out, s);
+  if (out_kind == 0)
+    return dr_out<OutF16>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
+  if (out_kind == 1)
+    return dr_out<OutBF16>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
+  return dr_out<OutF32>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
 }
 
 }  // namespace zpp

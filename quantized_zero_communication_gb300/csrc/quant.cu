@@ -153,18 +153,19 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
 }
 
 // K3: per source rank r, output slice position p = l_d*N + n_d holds original slice
-// j = n_d*M + l_d. Grid (tile group, p, r): each warp owns one warp tile of slice p of
-// rank r (the last tile of a slice may be short but always holds whole blocks).
+// j = n_d*M + l_d. Grid (tile group, p - p_begin, r): each warp owns one warp tile of
+// slice p of rank r (the last tile of a slice may be short but always holds whole
+// blocks). A launch may cover only the slices of some hop-1 chunks (p_begin = l_begin*N).
 template <typename TT, int BITS, int B>
 __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __restrict__ grads,
-                                                            int64_t E, int N, int M,
+                                                            int64_t E, int N, int M, int p_begin,
                                                             uint8_t* __restrict__ codes,
                                                             float* __restrict__ scales) {
   constexpr int TILE = QuantTile<B>::TILE;
   const int lane = threadIdx.x & 31;
   const int64_t k = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
-  const int p = blockIdx.y, r = blockIdx.z;
+  const int p = p_begin + static_cast<int>(blockIdx.y), r = blockIdx.z;
   if (k * TILE < S) {
     const int l_d = p / N, n_d = p - l_d * N;
     const int64_t j = static_cast<int64_t>(n_d) * M + l_d;
@@ -191,13 +192,15 @@ static cudaError_t run_quant(const void* x, int64_t n, void* codes, float* scale
 }
 
 template <typename TT, int BITS, int B>
-static cudaError_t run_reorder_quant(const void* g, int64_t E, int N, int M, void* codes,
-                                     float* scales, cudaStream_t s) {
+static cudaError_t run_reorder_quant(const void* g, int64_t E, int N, int M, int l_begin, int l_end,
+                                     void* codes, float* scales, cudaStream_t s) {
   auto kern = k_reorder_quant<TT, BITS, B>;
   const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
   const int64_t tps = (S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
-  const dim3 grid(tile_grid(tps, kWarps), static_cast<unsigned>(W), static_cast<unsigned>(W));
-  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(g), E, N, M,
+  // output slice positions of chunks l_begin .. l_end-1: p in [l_begin*N, l_end*N)
+  const dim3 grid(tile_grid(tps, kWarps), static_cast<unsigned>((l_end - l_begin) * N),
+                  static_cast<unsigned>(W));
+  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(g), E, N, M, l_begin * N,
                                  static_cast<uint8_t*>(codes), scales);
   return cudaGetLastError();
 }
@@ -232,9 +235,10 @@ cudaError_t launch_quant(const void* x, int is_bf16, int64_t n, int block, int b
 }
 
 cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block, int bits,
-                                 int N, int M, void* codes, float* scales, cudaStream_t s) {
+                                 int N, int M, int l_begin, int l_end, void* codes, float* scales,
+                                 cudaStream_t s) {
   return by_type_bits_block(is_bf16, bits, block, [&]<typename TT, int BITS, int B>() {
-    return run_reorder_quant<TT, BITS, B>(grads, E, N, M, codes, scales, s);
+    return run_reorder_quant<TT, BITS, B>(grads, E, N, M, l_begin, l_end, codes, scales, s);
   });
 }
 

@@ -55,6 +55,12 @@ zpp_status check_topology(int64_t E, int32_t block, int32_t bits, zpp_topology t
   return ZPP_OK;
 }
 
+bool valid_range(zpp_local_range r, zpp_topology t) {
+  return r.begin >= 0 && r.begin <= r.end && r.end <= t.gpus_per_node;
+}
+
+zpp_local_range full_range(zpp_topology t) { return zpp_local_range{0, t.gpus_per_node}; }
+
 }  // namespace
 
 extern "C" {
@@ -103,68 +109,92 @@ zpp_status zpp_dequant_blockwise(const void* codes, const float* scales, int64_t
   return from_cuda(zpp::launch_dequant(codes, scales, n, block, bits, y, static_cast<int>(y_dt), stream));
 }
 
-zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
-                                 int32_t block, int32_t bits, zpp_topology topo, void* codes,
-                                 float* scales, cudaStream_t stream) {
+zpp_status zpp_qgz_reorder_quant_range(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
+                                       int32_t block, int32_t bits, zpp_topology topo,
+                                       zpp_local_range range, void* codes, float* scales,
+                                       cudaStream_t stream) {
   int64_t W = 0;
   zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
   if (st != ZPP_OK) return st;
   if (g_dt != ZPP_F16 && g_dt != ZPP_BF16 && g_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
-  if (elems_per_rank == 0) return ZPP_OK;
+  if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!grads || !codes || !scales) return ZPP_ERR_INVALID_ARG;
   if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
   if (!aligned(grads, 32) || !aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_reorder_quant(grads, g_dt == ZPP_BF16, elems_per_rank, block, bits,
-                                             topo.num_nodes, topo.gpus_per_node, codes, scales,
-                                             stream));
+                                             topo.num_nodes, topo.gpus_per_node, range.begin,
+                                             range.end, codes, scales, stream));
 }
 
-zpp_status zpp_dequant_reduce_requant(const void* codes, const float* scales,
-                                      int64_t elems_per_rank, int32_t block, int32_t bits,
-                                      zpp_topology topo, void* out_codes, float* out_scales,
-                                      cudaStream_t stream) {
+zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
+                                 int32_t block, int32_t bits, zpp_topology topo, void* codes,
+                                 float* scales, cudaStream_t stream) {
+  return zpp_qgz_reorder_quant_range(grads, g_dt, elems_per_rank, block, bits, topo,
+                                     full_range(topo), codes, scales, stream);
+}
+
+zpp_status zpp_dequant_reduce_requant_range(const void* codes, const float* scales,
+                                            int64_t elems_per_rank, int32_t block, int32_t bits,
+                                            zpp_topology topo, zpp_local_range range,
+                                            void* out_codes, float* out_scales,
+                                            cudaStream_t stream) {
   int64_t W = 0;
   zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
   if (st != ZPP_OK) return st;
-  if (elems_per_rank == 0) return ZPP_OK;
+  if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!codes || !scales || !out_codes || !out_scales) return ZPP_ERR_INVALID_ARG;
   if (!aligned(codes, 32) || !aligned(out_codes, 32) || !aligned(scales, 4) ||
       !aligned(out_scales, 4))
     return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits,
                                                       topo.num_nodes, topo.gpus_per_node,
-                                                      out_codes, out_scales, stream));
+                                                      range.begin, range.end, out_codes,
+                                                      out_scales, stream));
 }
 
-zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t elems_per_rank,
-                              int32_t block, int32_t bits, zpp_topology topo, float* out,
-                              cudaStream_t stream) {
+zpp_status zpp_dequant_reduce_requant(const void* codes, const float* scales,
+                                      int64_t elems_per_rank, int32_t block, int32_t bits,
+                                      zpp_topology topo, void* out_codes, float* out_scales,
+                                      cudaStream_t stream) {
+  return zpp_dequant_reduce_requant_range(codes, scales, elems_per_rank, block, bits, topo,
+                                          full_range(topo), out_codes, out_scales, stream);
+}
+
+zpp_status zpp_dequant_reduce_scaled_range(const void* codes, const float* scales,
+                                           int64_t elems_per_rank, int32_t block, int32_t bits,
+                                           zpp_topology topo, zpp_local_range range,
+                                           float post_scale, void* out, zpp_dtype out_dt,
+                                           cudaStream_t stream) {
   int64_t W = 0;
   zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
   if (st != ZPP_OK) return st;
-  if (elems_per_rank == 0) return ZPP_OK;
+  if (out_dt != ZPP_F16 && out_dt != ZPP_BF16 && out_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (!(post_scale == post_scale) || post_scale - post_scale != 0.0f) return ZPP_ERR_INVALID_ARG;
+  if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
   if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
-                                              topo.num_nodes, topo.gpus_per_node, 1.0f, out,
-                                              ZPP_F32, stream));
+                                              topo.num_nodes, topo.gpus_per_node, range.begin,
+                                              range.end, post_scale, out,
+                                              static_cast<int>(out_dt), stream));
 }
 
 zpp_status zpp_dequant_reduce_scaled(const void* codes, const float* scales,
                                      int64_t elems_per_rank, int32_t block, int32_t bits,
                                      zpp_topology topo, float post_scale, void* out,
                                      zpp_dtype out_dt, cudaStream_t stream) {
-  int64_t W = 0;
-  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
-  if (st != ZPP_OK) return st;
-  if (out_dt != ZPP_F16 && out_dt != ZPP_BF16 && out_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
-  if (!(post_scale == post_scale) || post_scale - post_scale != 0.0f) return ZPP_ERR_INVALID_ARG;
-  if (elems_per_rank == 0) return ZPP_OK;
-  if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
-  if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
-  return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
-                                              topo.num_nodes, topo.gpus_per_node, post_scale, out,
-                                              static_cast<int>(out_dt), stream));
+  return zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, topo,
+                                         full_range(topo), post_scale, out, out_dt, stream);
+}
+
+zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t elems_per_rank,
+                              int32_t block, int32_t bits, zpp_topology topo, float* out,
+                              cudaStream_t stream) {
+  return zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, topo,
+                                         full_range(topo), 1.0f, out, ZPP_F32, stream);
 }
 
 zpp_status zpp_device_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream) {

@@ -15,21 +15,24 @@ cudaError_t launch_quant(const void* x, int is_bf16, int64_t n, int block, int b
 cudaError_t launch_dequant(const void* codes, const float* scales, int64_t n, int block,
                            int bits, void* y, int out_kind, cudaStream_t s);
 
+// The qgZ launchers cover the hop-1 chunks / receivers with local index l in
+// [l_begin, l_end) (the whole exchange is [0, M)).
 // K3: slice reorder + block quantisation of W = N*M ranks of E elements.
-cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block,
-                                 int bits, int N, int M, void* codes, float* scales,
+cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block, int bits,
+                                 int N, int M, int l_begin, int l_end, void* codes, float* scales,
                                  cudaStream_t s);
 
 // K4: intra-node fused dequantise -> fp32 sum over M chunks -> requantise.
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
-                                          int block, int bits, int N, int M, void* out_codes,
-                                          float* out_scales, cudaStream_t s);
+                                          int block, int bits, int N, int M, int l_begin,
+                                          int l_end, void* out_codes, float* out_scales,
+                                          cudaStream_t s);
 
 // K5: inter-node dequantise -> fp32 sum over N slices, times post_scale, stored as fp16
 // (out_kind 0), bf16 (1) or fp32 (2).
 cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, float post_scale, void* out, int out_kind,
-                                  cudaStream_t s);
+                                  int bits, int N, int M, int l_begin, int l_end, float post_scale,
+                                  void* out, int out_kind, cudaStream_t s);
 
 // K6: 256-bit device copy (the same-run HBM reference).
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s);

@@ -110,6 +110,18 @@ def test_qgz_entry_points_reject_bad_topologies():
         assert f(8 * 128, 128, 4, T(2, 4), FAKE + 16) == zb.ZPP_ERR_MISALIGNED
     assert zb.zpp_qgz_reorder_quant(FAKE, zb.ZPP_F32, 1024, 128, 4, T(2, 4), FAKE,
                                     FAKE) == zb.ZPP_ERR_UNSUPPORTED
+    R = zb.LocalRange
+    for lr, want in (((0, 4), zb.ZPP_OK), ((2, 2), zb.ZPP_OK), ((-1, 2), zb.ZPP_ERR_INVALID_ARG),
+                     ((3, 2), zb.ZPP_ERR_INVALID_ARG), ((0, 5), zb.ZPP_ERR_INVALID_ARG)):
+        rng = R(*lr)
+        if want == zb.ZPP_OK and lr[0] != lr[1]:
+            continue  # a non-empty valid range would launch: not on fake addresses
+        assert zb.zpp_qgz_reorder_quant_range(FAKE, zb.ZPP_BF16, 1024, 128, 4, T(2, 4), rng,
+                                              FAKE, FAKE) == want
+        assert zb.zpp_dequant_reduce_requant_range(FAKE, FAKE, 1024, 128, 4, T(2, 4), rng, FAKE,
+                                                   FAKE) == want
+        assert zb.zpp_dequant_reduce_scaled_range(FAKE, FAKE, 1024, 128, 4, T(2, 4), rng, 1.0,
+                                                  FAKE, 2) == want
     sc = zb.zpp_dequant_reduce_scaled
     assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE, 5) == zb.ZPP_ERR_INVALID_ARG
     assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), float("nan"), FAKE, 2) == zb.ZPP_ERR_INVALID_ARG

@@ -220,6 +220,26 @@ def test_averaged_owner_slices(N, M, bits):
     assert torch.equal(one, plain)
 
 
+@pytest.mark.parametrize("N,M", [(2, 4), (3, 2), (1, 8), (4, 8)])
+@pytest.mark.parametrize("n_streams", [1, 2, 3])
+def test_pipelined_subexchanges_equal_the_whole(N, M, n_streams):
+    """The local-index sub-pipelines on several streams give the same buffers, bit for bit,
+    as the three unrestricted calls."""
+    W, B, bits = N * M, 512, 4
+    E = W * 2 * 4096
+    g = inputs.draw("laplace", W * E, seed=31 * W + n_streams, dtype=torch.bfloat16,
+                    device=DEV).reshape(W, E)
+    bufs = zpp.qgz_pipelined(g, B, bits, N, M, n_streams=n_streams)
+    whole = run_qgz(g, B, bits, N, M)
+    split = zpp.qgz_pipelined(g, B, bits, N, M, chunks=n_streams, streams=(
+        "split", torch.cuda.Stream(DEV), torch.cuda.Stream(DEV, priority=-1)))
+    for a, b in zip([host(t) for t in (split.c0, split.s0, split.c1, split.s1, split.out)], whole):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    got = [host(t) for t in (bufs.c0, bufs.s0, bufs.c1, bufs.s1, bufs.out)]
+    for a, b in zip(got, whole):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
 def test_qgz_fp16_gradients():
     g = inputs.draw("normal", 8 * 8 * 1024, seed=4, dtype=torch.float16, device=DEV).reshape(8, -1)
     check_qgz(g, 128, 4, 2, 4)
