@@ -422,9 +422,9 @@ def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, 
             bytes_step, world):
     """The same step through the public API with host buffers: every step copies the
     weights and gradients in from pinned host memory and copies the dequantised weights
-    and the reduced gradient slices back out. The qwZ half (weights) and the qgZ half
-    (gradients) are independent, so they run on two streams: one half's host-to-device
-    copy overlaps the other's device-to-host copy and kernels."""
+    and the reduced gradient slices back out. The weight half runs on the caller's stream;
+    the gradient half runs on a second stream and starts its upload once the weights are
+    on the device, so the weights' copy back overlaps the gradients' copy in."""
     N, M = QGZ_N, QGZ_M
 
     def pinned(t):
@@ -437,19 +437,19 @@ def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, 
     sb = torch.cuda.Stream(dev)
 
     def step():
-        fork = torch.cuda.Event()
-        fork.record(sa)
-        sb.wait_event(fork)
+        x.copy_(hx, non_blocking=True)  # qwZ on the caller's stream: weights in and out
+        x_in = torch.cuda.Event()
+        x_in.record(sa)
+        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
+        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
+        hy.copy_(y, non_blocking=True)
+        sb.wait_event(x_in)
         with torch.cuda.stream(sb):  # qgZ: gradients in, owner slices out
             g.copy_(hg, non_blocking=True)
             zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
             zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
             zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
             hout.copy_(out, non_blocking=True)
-        x.copy_(hx, non_blocking=True)  # qwZ on the caller's stream: weights in and out
-        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
-        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
-        hy.copy_(y, non_blocking=True)
         join = torch.cuda.Event()
         join.record(sb)
         sa.wait_event(join)

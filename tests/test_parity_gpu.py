@@ -343,6 +343,32 @@ def test_largest_sweep_size(bits):
     assert np.array_equal(host(s1).view(np.uint32), os1.view(np.uint32))
 
 
+@pytest.mark.slow
+def test_offsets_beyond_2_pow_31():
+    """n = 2^31 + 2^20 + 77 fp16 elements (4.3 GB): quant and dequant through 64-bit offsets.
+    Quantisation is block-local, so the oracle checks windows of whole blocks one by one:
+    the start, both sides of element 2^31, and the ragged tail."""
+    n, B = (1 << 31) + (1 << 20) + 77, 1024
+    x = torch.empty(n, dtype=torch.float16, device=DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(2024)
+    for i in range(0, n, 1 << 28):  # draw in pieces to bound the fp32 temporary
+        m = min(1 << 28, n - i)
+        x[i:i + m] = (torch.randn(m, generator=g, device=DEV) * 0.02).half()
+    codes, scales = zpp.quant_blockwise(x, B, 8)
+    y = zpp.dequant_blockwise(codes, scales, n, B, 8, torch.float16)
+    torch.cuda.synchronize()
+    for lo in (0, (1 << 31) - 64 * B, n - (n % B) - 64 * B):
+        hi = min(n, lo + 128 * B)
+        xb = bits16(x[lo:hi])
+        oc, os_ = oracle.quant_blockwise(xb, oracle.F16, B, 8)
+        assert np.array_equal(codes[lo:hi].cpu().numpy(), oc), lo
+        assert np.array_equal(scales[lo // B:(hi + B - 1) // B].cpu().numpy().view(np.uint32),
+                              os_.view(np.uint32)), lo
+        assert np.array_equal(bits16(y[lo:hi]), oracle.dequant_blockwise(oc, os_, hi - lo, B, 8,
+                                                                         oracle.F16)), lo
+
+
 def test_device_copy():
     a = torch.randint(0, 255, (1 << 20,), dtype=torch.uint8, device=DEV)
     b = torch.zeros_like(a)
