@@ -380,8 +380,7 @@ def _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out, per_kernel_bytes, r
     ALU-bound fused hop overlaps another chunk's memory-bound reorder+quantise."""
     N, M = QGZ_N, QGZ_M
     stream = torch.cuda.current_stream(dev)
-    bufs = zpp.QgzBuffers.__new__(zpp.QgzBuffers)
-    bufs.c0, bufs.s0, bufs.c1, bufs.s1, bufs.out = c0, s0, c1, s1, out
+    bufs = zpp.QgzBuffers(c0, s0, c1, s1, out)
     qbytes = sum(per_kernel_bytes[k] for k in KERNELS[2:])
 
     def serial():

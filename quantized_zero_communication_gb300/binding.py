@@ -263,17 +263,21 @@ def dequant_reduce_scaled(codes, scales, E, block, bits, N, M, post_scale=None, 
 
 
 class QgzBuffers:
-    """Device buffers of one qgZ exchange: reordered codes/scales, hop-1 codes/scales and
-    the owner slices."""
+    """Device buffers of one qgZ exchange: reordered codes/scales (c0, s0), hop-1
+    codes/scales (c1, s1) and the owner slices (out)."""
 
-    def __init__(self, W, E, block, bits, M, device, out_dtype=None):
+    def __init__(self, c0, s0, c1, s1, out):
+        self.c0, self.s0, self.c1, self.s1, self.out = c0, s0, c1, s1, out
+
+    @classmethod
+    def allocate(cls, W, E, block, bits, M, device, out_dtype=None):
         torch = _torch()
         C = E // M
-        self.c0 = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=device)
-        self.s0 = torch.empty((W, E // block), dtype=torch.float32, device=device)
-        self.c1 = torch.empty((W, zpp_code_bytes(C, bits)), dtype=torch.uint8, device=device)
-        self.s1 = torch.empty((W, C // block), dtype=torch.float32, device=device)
-        self.out = torch.empty((W, E // W), dtype=out_dtype or torch.float32, device=device)
+        return cls(torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=device),
+                   torch.empty((W, E // block), dtype=torch.float32, device=device),
+                   torch.empty((W, zpp_code_bytes(C, bits)), dtype=torch.uint8, device=device),
+                   torch.empty((W, C // block), dtype=torch.float32, device=device),
+                   torch.empty((W, E // W), dtype=out_dtype or torch.float32, device=device))
 
 
 def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=None,
@@ -292,7 +296,7 @@ def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=N
     W = N * M
     E = grads.numel() // W
     if bufs is None:
-        bufs = QgzBuffers(W, E, block, bits, M, grads.device)
+        bufs = QgzBuffers.allocate(W, E, block, bits, M, grads.device)
     main = torch.cuda.current_stream(grads.device)
     if streams is None:
         streams = [torch.cuda.Stream(grads.device) for _ in range(min(n_streams, M))]
