@@ -57,7 +57,7 @@ MUTANTS = [
 
 def _copy_repo(dst):
     def ignore(path, names):
-        return {n for n in names if n in (".git", "_work", "__pycache__", "_build",
+        return {n for n in names if n in (".git", "__pycache__", "_build",
                                           ".pytest_cache") or n.endswith((".so", ".o"))}
     for d in ("oracle", "tests", "quantized_zero_communication_gb300"):
         shutil.copytree(os.path.join(ROOT, d), os.path.join(dst, d), ignore=ignore)
