@@ -336,7 +336,7 @@ def run_ours(args):
         result["only"] = active[0]
     if not args.no_e2e and not args.only:
         result["e2e"] = run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1,
-                                out, n_qwz, E, bytes_step, world)
+                                out, n_qwz, E, bytes_step, world, pieces=args.e2e_pieces)
     B.clear()
     if not args.only:
         del x, g, codes, scales, y, c0, s0, c1, s1, out
@@ -418,40 +418,64 @@ def _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out, per_kernel_bytes, r
 
 
 def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, n_qwz, E,
-            bytes_step, world):
+            bytes_step, world, pieces=2):
     """The same step through the public API with host buffers: every step copies the
     weights and gradients in from pinned host memory and copies the dequantised weights
-    and the reduced gradient slices back out. The weight half runs on the caller's stream;
-    the gradient half runs on a second stream and starts its upload once the weights are
-    on the device, so the weights' copy back overlaps the gradients' copy in."""
+    and the reduced gradient slices back out. All host-to-device copies run in order on one
+    input stream -- the weights in `pieces` block-aligned pieces (each its own pinned
+    allocation), then the gradients; each weight piece is quantised, dequantised and copied
+    back on a second stream as soon as it has arrived, and the gradient half runs on a
+    third, so copies back overlap the copies in of later data."""
     N, M = QGZ_N, QGZ_M
+    per = n_qwz // pieces
+    assert per % QWZ_BLOCK == 0 and per * pieces == n_qwz
+    nb = per // QWZ_BLOCK
 
-    def pinned(t):
-        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    def pinned(shape, dtype):
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
 
-    hx, hg, hy, hout = pinned(x), pinned(g), pinned(y), pinned(out)
-    hx.copy_(x)
+    hx = [pinned((per,), x.dtype) for _ in range(pieces)]
+    hy = [pinned((per,), y.dtype) for _ in range(pieces)]
+    for i in range(pieces):
+        hx[i].copy_(x[i * per:(i + 1) * per])
+    hg, hout = pinned(g.shape, g.dtype), pinned(out.shape, out.dtype)
     hg.copy_(g)
-    sa = torch.cuda.current_stream(dev)
-    sb = torch.cuda.Stream(dev)
+    main = torch.cuda.current_stream(dev)
+    s_in, s_w, s_g = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def step():
-        x.copy_(hx, non_blocking=True)  # qwZ on the caller's stream: weights in and out
-        x_in = torch.cuda.Event()
-        x_in.record(sa)
-        zpp.quant_blockwise(x, QWZ_BLOCK, QWZ_BITS, codes, scales)
-        zpp.dequant_blockwise(codes, scales, n_qwz, QWZ_BLOCK, QWZ_BITS, y=y)
-        hy.copy_(y, non_blocking=True)
-        sb.wait_event(x_in)
-        with torch.cuda.stream(sb):  # qgZ: gradients in, owner slices out
+        fork = torch.cuda.Event()
+        fork.record(main)
+        for st in (s_in, s_w, s_g):
+            st.wait_event(fork)
+        arrived = []
+        with torch.cuda.stream(s_in):
+            for i in range(pieces):
+                x[i * per:(i + 1) * per].copy_(hx[i], non_blocking=True)
+                arrived.append(torch.cuda.Event())
+                arrived[-1].record(s_in)
             g.copy_(hg, non_blocking=True)
+            g_in = torch.cuda.Event()
+            g_in.record(s_in)
+        with torch.cuda.stream(s_w):  # qwZ: each weight piece as soon as it is on the device
+            for i in range(pieces):
+                lo, hi = i * per, (i + 1) * per
+                s_w.wait_event(arrived[i])
+                zpp.quant_blockwise(x[lo:hi], QWZ_BLOCK, QWZ_BITS, codes[lo:hi],
+                                    scales[i * nb:(i + 1) * nb])
+                zpp.dequant_blockwise(codes[lo:hi], scales[i * nb:(i + 1) * nb], per, QWZ_BLOCK,
+                                      QWZ_BITS, y=y[lo:hi])
+                hy[i].copy_(y[lo:hi], non_blocking=True)
+        with torch.cuda.stream(s_g):  # qgZ: once the gradients are on the device
+            s_g.wait_event(g_in)
             zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
             zpp.dequant_reduce_requant(c0, s0, E, QGZ_BLOCK, QGZ_BITS, N, M, c1, s1)
             zpp.dequant_reduce(c1, s1, E, QGZ_BLOCK, QGZ_BITS, N, M, out)
             hout.copy_(out, non_blocking=True)
-        join = torch.cuda.Event()
-        join.record(sb)
-        sa.wait_event(join)
+        for st in (s_in, s_w, s_g):
+            join = torch.cuda.Event()
+            join.record(st)
+            main.wait_event(join)
 
     steps = max(3, min(args.steps, args.e2e_steps))
     for _ in range(3):
@@ -459,17 +483,17 @@ def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, 
     torch.cuda.synchronize()
     barrier()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(sa)
+    s.record(main)
     for _ in range(steps):
         step()
-    e.record(sa)
+    e.record(main)
     torch.cuda.synchronize()
     ms = max_over_ranks(s.elapsed_time(e), device=dev)
-    h2d = hx.numel() * hx.element_size() + hg.numel() * hg.element_size()
-    d2h = hy.numel() * hy.element_size() + hout.numel() * hout.element_size()
+    h2d = sum(t.numel() * t.element_size() for t in (*hx, hg))
+    d2h = sum(t.numel() * t.element_size() for t in (*hy, hout))
     return {"value": round(world * bytes_step * steps / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(ms / steps, 3), "streams": 2}
+            "ms_per_step": round(ms / steps, 3), "streams": 3, "weight_pieces": pieces}
 
 
 # ----------------------------------------------------------------------------- oracle legs
@@ -575,6 +599,8 @@ def main(argv=None):
                     help="time one kernel of the step on the full workload, keeping only its "
                          "own buffers on the device (profiling runs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-pieces", type=int, default=2,
+                    help="weight pieces of the end-to-end leg (1, 2, 4 or 8)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
