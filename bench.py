@@ -587,6 +587,75 @@ def run_reference(args):
     return result
 
 
+def run_sweep(args):
+    """Times K1, K2 and the fused K-way hop (topology 1 x K, K in {2, 8, 16}) over the
+    sweep's sizes x dtypes x bits x blocks (N(0, 0.02) data; timing does not depend on the
+    values), 20 event-timed launches each after 3 warm-up ones, L2 larger than nothing:
+    sizes below the 129 MB L2 are flushed by a 256 MiB write between launches."""
+    import torch
+    import quantized_zero_communication_gb300 as zpp
+    from quantized_zero_communication_gb300 import build as zbuild, inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if not os.path.exists(zbuild.LIB):
+        zbuild.build()
+    peak, peak_src = hbm_peak()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn, small):
+        for _ in range(3):
+            fn()
+        tot = 0.0
+        for _ in range(20):
+            if small:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / 20 * 1e-3
+
+    rows = []
+    for size in inputs.SWEEP_SIZES:
+        for dt in inputs.SWEEP_DTYPES:
+            x = inputs.draw("normal", size, seed=100, dtype=dt, device=dev)
+            for bits in inputs.SWEEP_BITS:
+                for block in inputs.SWEEP_BLOCKS:
+                    cb, ns = code_bytes(size, bits), math.ceil(size / block)
+                    codes, scales = zpp.quant_blockwise(x, block, bits)
+                    y = torch.empty_like(x)
+                    small = 2 * size < L2_BYTES * 2
+                    t1 = timed(lambda: zpp.quant_blockwise(x, block, bits, codes, scales), small)
+                    t2 = timed(lambda: zpp.dequant_blockwise(codes, scales, size, block, bits, y=y),
+                               small)
+                    b12 = 2 * size + cb + 4 * ns
+                    row = {"size": size, "dtype": str(dt).replace("torch.", ""), "bits": bits,
+                           "block": block,
+                           "quant_us": round(t1 * 1e6, 1), "quant_frac": round(b12 / t1 / 1e9 / peak, 3),
+                           "dequant_us": round(t2 * 1e6, 1), "dequant_frac": round(b12 / t2 / 1e9 / peak, 3)}
+                    if dt == torch.bfloat16:
+                        for K in (2, 8, 16):
+                            E = size // K
+                            if E % (K * block):
+                                continue
+                            c0, s0 = zpp.qgz_reorder_quant(x.view(K, E), block, bits, 1, K)
+                            c1, s1 = zpp.dequant_reduce_requant(c0, s0, E, block, bits, 1, K)
+                            t4 = timed(lambda: zpp.dequant_reduce_requant(c0, s0, E, block, bits, 1,
+                                                                          K, c1, s1), small)
+                            b4 = (cb + 4 * ns) * (1 + 1 / K)
+                            row[f"drr_K{K}_us"] = round(t4 * 1e6, 1)
+                            row[f"drr_K{K}_frac"] = round(b4 / t4 / 1e9 / peak, 3)
+                            del c0, s0, c1, s1
+                    rows.append(row)
+                    del codes, scales, y
+            del x
+            torch.cuda.empty_cache()
+    print(json.dumps({"sweep": rows, "peak": peak, "peak_source": peak_src}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,6 +664,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--size-div", type=int, default=1,
                     help="shrink the workload by this power of two (profiling runs only)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time quant, dequant and the fused hop over the sweep's sizes, dtypes, "
+                         "widths and blocks (one JSON object; not the benchmark line)")
     ap.add_argument("--only", choices=("K1", "K2", "K3", "K4", "K5"),
                     help="time one kernel of the step on the full workload, keeping only its "
                          "own buffers on the device (profiling runs)")
@@ -613,6 +685,8 @@ def main(argv=None):
         ap.error("--size-div must be a power of two <= 1024")
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 
