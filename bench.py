@@ -75,7 +75,7 @@ def workload_sizes(div):
 def workload_config(div, n_qwz, E):
     return {
         "workload": "qwZ GPT layer (hidden 8192: 805,306,368 fp16 weights, 16 virtual ranks, "
-                    "INT8 block 2048) + qGZ gradient bucket (536,870,912 bf16 over 4 nodes x "
+                    "INT8 block 2048) + qgZ gradient bucket (536,870,912 bf16 over 4 nodes x "
                     "8 GPUs, INT4 block 512, K=8 then K=4)" + (f", sizes / {div}" if div > 1 else ""),
         "qwz_elements": n_qwz, "qwz_block": QWZ_BLOCK, "qwz_bits": QWZ_BITS, "qwz_ranks": 16,
         "qgz_elements": QGZ_N * QGZ_M * E, "qgz_topology": [QGZ_N, QGZ_M],
