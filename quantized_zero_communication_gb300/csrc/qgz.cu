@@ -8,7 +8,10 @@
 // (n', l), n' = 0..N-1, dequantises and sums into its fp32 owner slice.
 //
 // A K4 lane reads 16 code bytes per source (32 INT4 or 16 INT8 elements); a K5 lane owns
-// 16 elements. Sums live in registers as fp32 pairs (2j, 2j+1).
+// 16 elements. Sums live in registers as fp32 pairs, four pairs per code word k: elements
+// (8k+2j, 8k+2j+1) -- except the INT4 words that K4 converts by the split integer / fp32
+// path (k < kSplitWords), whose pairs hold (8k, 8k+2), (8k+4, 8k+6), (8k+1, 8k+3),
+// (8k+5, 8k+7).
 //
 // Pages: "ZeRO++: Extremely Efficient Collective Communication for Large Model Training"
 // (atlas.scime.ai summary), Approach: 2-hop all-to-all INT4 gradient reduction that
@@ -22,6 +25,15 @@ namespace zpp {
 
 // Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
 // in K5; a CTA tile is 8 warps x one row.
+// K4 with INT4 codes and M a multiple of a chunk of 4 or 8 sources runs as
+// k_dequant_reduce_requant_split: kSplitWords of the 4 code words per source are converted
+// by int4x8_to_f2_eo (which shares the conversion between the integer and fp32 pipes),
+// under a register budget of kSplitMinCtas CTAs of 256 threads per SM. Measured on GB300
+// (4 x 8 bucket, K = 8) this pair is the fastest; with 2 sources per chunk the kernel is
+// nearer its memory bound and the plain conversion is faster.
+constexpr int kSplitWords = 3;
+constexpr int kSplitMinCtas = 3;
+
 template <int BITS>
 struct Geo4 {
   static constexpr int EPL = BITS == 4 ? 32 : 16;  // elements per lane
@@ -33,9 +45,10 @@ constexpr int kEpl5 = 16;
 constexpr int kRow5 = 32 * kEpl5;
 constexpr int kCta5 = kWarps * kRow5;
 
-// acc (fp32 pairs (2j, 2j+1)) += q * s for the 16 code bytes of one source: each term
-// added with one rounding (fused multiply-add), in the order the sources are visited.
-template <int BITS, int NWORDS>
+// acc += q * s for the 16 code bytes of one source: each term added with one rounding
+// (fused multiply-add), in the order the sources are visited. INT4 words k < SPLIT take
+// the split conversion (and its pair layout).
+template <int BITS, int NWORDS, int SPLIT>
 __device__ __forceinline__ void accumulate(f32x2* acc, const uint32_t* w, float s) {
   const f32x2 ss = f2(s, s);
 #pragma unroll
@@ -45,6 +58,13 @@ __device__ __forceinline__ void accumulate(f32x2* acc, const uint32_t* w, float 
       int8x4_to_f2(w[k], q);
       acc[2 * k] = f2_fma(q[0], ss, acc[2 * k]);
       acc[2 * k + 1] = f2_fma(q[1], ss, acc[2 * k + 1]);
+    } else if (k < SPLIT) {
+      f32x2 ev[2], od[2];
+      int4x8_to_f2_eo(w[k], ev, od);
+      acc[4 * k] = f2_fma(ev[0], ss, acc[4 * k]);
+      acc[4 * k + 1] = f2_fma(ev[1], ss, acc[4 * k + 1]);
+      acc[4 * k + 2] = f2_fma(od[0], ss, acc[4 * k + 2]);
+      acc[4 * k + 3] = f2_fma(od[1], ss, acc[4 * k + 3]);
     } else {
       f32x2 q[4];
       int4x8_to_f2(w[k], q);
@@ -56,7 +76,7 @@ __device__ __forceinline__ void accumulate(f32x2* acc, const uint32_t* w, float 
 
 // Sum over K sources at a constant stride, KC loads in flight per chunk. EXACT: K is a
 // multiple of KC (no per-source test); LIVE: this lane has data (else it loads nothing).
-template <int BITS, int NWORDS, int KC, bool EXACT>
+template <int BITS, int NWORDS, int SPLIT, int KC, bool EXACT>
 __device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase, int64_t cstep,
                                                const float* sbase, int64_t sstep, int K, bool live) {
   for (int k0 = 0; k0 < K; k0 += KC) {
@@ -82,7 +102,7 @@ __device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase,
     }
 #pragma unroll
     for (int i = 0; i < KC; ++i)
-      if (EXACT || k0 + i < K) accumulate<BITS, NWORDS>(acc, raw[i], s[i]);
+      if (EXACT || k0 + i < K) accumulate<BITS, NWORDS, SPLIT>(acc, raw[i], s[i]);
   }
 }
 
@@ -90,7 +110,7 @@ __device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase,
 // x one row each -- so no thread divides to find its work. A launch may cover only the
 // receivers whose local index l lies in [l_begin, l_begin + gridDim.y). Blocks wider than a row are reduced
 // across the warps that share them through shared memory.
-template <int BITS, int KC, bool EXACT, bool FULL>
+template <int BITS, int KC, bool EXACT, bool FULL, int SPLIT>
 __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
                                          const float* __restrict__ scales, int64_t E, int log2b,
                                          int M, int l_begin, uint8_t* __restrict__ out_codes,
@@ -112,7 +132,7 @@ __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
   f32x2 acc[G::NP];
 #pragma unroll
   for (int j = 0; j < G::NP; ++j) acc[j] = f2(0.0f, 0.0f);
-  reduce_sources<BITS, 4, KC, EXACT>(acc, cbase, cb_in, sbase, sc_in, M, valid);
+  reduce_sources<BITS, 4, SPLIT, KC, EXACT>(acc, cbase, cb_in, sbase, sc_in, M, valid);
 
   float m = 0.0f;
 #pragma unroll
@@ -144,11 +164,26 @@ __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
     } else {
       const f32x2 q[4] = {round_codes(acc[4 * k], iv2), round_codes(acc[4 * k + 1], iv2),
                           round_codes(acc[4 * k + 2], iv2), round_codes(acc[4 * k + 3], iv2)};
-      w[k] = pack_int4x8(q);
+      w[k] = k < SPLIT ? pack_int4x8_eo(q) : pack_int4x8(q);
     }
   }
   st_v4(out_codes + r * cb_out + e * BITS / 8, make_uint4(w[0], w[1], w[2], w[3]));
   if ((e & (B - 1)) == 0) out_scales[r * sc_out + (e >> log2b)] = sc;
+}
+
+template <int BITS, int KC, bool EXACT, int SPLIT>
+__device__ __forceinline__ void drr_body(const uint8_t* __restrict__ codes,
+                                         const float* __restrict__ scales, int64_t E, int log2b,
+                                         int M, int l_begin, uint8_t* __restrict__ out_codes,
+                                         float* __restrict__ out_scales) {
+  __shared__ float red[kWarps];
+  const int64_t C = E / M;
+  if ((static_cast<int64_t>(blockIdx.x) + 1) * Geo4<BITS>::CTA <= C)  // CTA-uniform
+    drr_tile<BITS, KC, EXACT, true, SPLIT>(codes, scales, E, log2b, M, l_begin, out_codes,
+                                           out_scales, red);
+  else
+    drr_tile<BITS, KC, EXACT, false, SPLIT>(codes, scales, E, log2b, M, l_begin, out_codes,
+                                            out_scales, red);
 }
 
 template <int BITS, int KC, bool EXACT>
@@ -156,12 +191,16 @@ __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce_requant(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                              int64_t E, int log2b, int M, int l_begin,
                              uint8_t* __restrict__ out_codes, float* __restrict__ out_scales) {
-  __shared__ float red[kWarps];
-  const int64_t C = E / M;
-  if ((static_cast<int64_t>(blockIdx.x) + 1) * Geo4<BITS>::CTA <= C)  // CTA-uniform
-    drr_tile<BITS, KC, EXACT, true>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales, red);
-  else
-    drr_tile<BITS, KC, EXACT, false>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales, red);
+  drr_body<BITS, KC, EXACT, 0>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales);
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kThreads, kSplitMinCtas)
+    k_dequant_reduce_requant_split(const uint8_t* __restrict__ codes,
+                                   const float* __restrict__ scales, int64_t E, int log2b, int M,
+                                   int l_begin, uint8_t* __restrict__ out_codes,
+                                   float* __restrict__ out_scales) {
+  drr_body<4, KC, true, kSplitWords>(codes, scales, E, log2b, M, l_begin, out_codes, out_scales);
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
@@ -188,8 +227,8 @@ __global__ void __launch_bounds__(kThreads)
   f32x2 acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = f2(0.0f, 0.0f);
-  reduce_sources<BITS, NW, KC, EXACT>(acc, cbase, static_cast<int64_t>(M) * cb, sbase,
-                                      static_cast<int64_t>(M) * sc, N, true);
+  reduce_sources<BITS, NW, 0, KC, EXACT>(acc, cbase, static_cast<int64_t>(M) * cb, sbase,
+                                         static_cast<int64_t>(M) * sc, N, true);
   const f32x2 ps = f2(post_scale, post_scale);
   float v[16];
 #pragma unroll
@@ -206,12 +245,15 @@ static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, in
   const dim3 grid(tile_grid(E / M, Geo4<BITS>::CTA), le - lb, N);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
-  if (M % KC == 0)
-    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, oc,
-                                                                       out_scales);
+  if (M % KC != 0)
+    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb,
+                                                                        oc, out_scales);
+  else if constexpr (BITS == 4 && KC >= 4)
+    k_dequant_reduce_requant_split<KC><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, oc,
+                                                                 out_scales);
   else
-    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, oc,
-                                                                        out_scales);
+    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb,
+                                                                       oc, out_scales);
   return cudaGetLastError();
 }
 

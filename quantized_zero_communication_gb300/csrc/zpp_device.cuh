@@ -178,6 +178,12 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
   return r;
 }
+// As f2_fma, rounded toward zero.
+__device__ __forceinline__ f32x2 f2_fma_rz(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 
 // ---------------------------------------------------------------------------------
 // Exact integer <-> float conversions without the conversion unit.
@@ -208,6 +214,28 @@ __device__ __forceinline__ void int4x8_to_f2(uint32_t w, f32x2 q[4]) {
   for (int j = 0; j < 4; ++j) q[j] = f2_add(f2(byte_to_magic(lo, j), byte_to_magic(hi, j)), off);
 }
 
+// Eight INT4 codes -> exact floats, with the work split between the integer pipe and the
+// fp32 pipe: one byte permute per byte (two codes) instead of one per code. With
+// u = w ^ 0x88888888, byte j of u holds b = (q_2j + 8) + 16 (q_2j+1 + 8), and the permute
+// gives the float B = 2^23 + b. Then, every step exact:
+//   h      = rz(B / 16 + (1.5*2^23 - 2^19)) = 1.5*2^23 + (q_2j+1 + 8)  (rz drops (b%16)/16)
+//   q_2j+1 = h - (1.5*2^23 + 8)
+//   q_2j   = (B - (2^23 + 136)) - 16 q_2j+1
+// ev[m] = (q_4m, q_4m+2), od[m] = (q_4m+1, q_4m+3), m = 0, 1.
+__device__ __forceinline__ void int4x8_to_f2_eo(uint32_t w, f32x2 ev[2], f32x2 od[2]) {
+  const uint32_t u = w ^ 0x88888888u;
+  const f32x2 sixteenth = f2(0.0625f, 0.0625f), hi_base = f2(12058624.0f, 12058624.0f);
+  const f32x2 hi_off = f2(-12582920.0f, -12582920.0f);  // -(1.5*2^23 + 8)
+  const f32x2 b_off = f2(-8388744.0f, -8388744.0f);     // -(2^23 + 136)
+  const f32x2 m16 = f2(-16.0f, -16.0f);
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const f32x2 b = f2(byte_to_magic(u, 2 * m), byte_to_magic(u, 2 * m + 1));
+    od[m] = f2_add(f2_fma_rz(b, sixteenth, hi_base), hi_off);
+    ev[m] = f2_fma(od[m], m16, f2_add(b, b_off));
+  }
+}
+
 // Four INT8 codes (element i in byte i) -> two pairs (0,1), (2,3) of exact floats.
 __device__ __forceinline__ void int8x4_to_f2(uint32_t w, f32x2 q[2]) {
   const uint32_t u = w ^ 0x80808080u;              // q + 128 in every byte
@@ -230,6 +258,19 @@ __device__ __forceinline__ uint32_t pack_int4x8(const f32x2 r[4]) {
                                        __float_as_uint(v[4]), __float_as_uint(v[6]));
   const uint32_t od = gather_low_bytes(__float_as_uint(v[1]), __float_as_uint(v[3]),
                                        __float_as_uint(v[5]), __float_as_uint(v[7]));
+  return (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+}
+
+// Eight rounded magic floats in the layout of int4x8_to_f2_eo (pairs (0,2), (4,6),
+// (1,3), (5,7)) -> one INT4 word.
+__device__ __forceinline__ uint32_t pack_int4x8_eo(const f32x2 r[4]) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) f2_split(r[j], v[2 * j], v[2 * j + 1]);
+  const uint32_t ev = gather_low_bytes(__float_as_uint(v[0]), __float_as_uint(v[1]),
+                                       __float_as_uint(v[2]), __float_as_uint(v[3]));
+  const uint32_t od = gather_low_bytes(__float_as_uint(v[4]), __float_as_uint(v[5]),
+                                       __float_as_uint(v[6]), __float_as_uint(v[7]));
   return (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
 }
 

@@ -161,7 +161,8 @@ def test_qwz_round_trip_workload():
 
 
 # ----------------------------------------------------------------------- qgZ (K3, K4, K5)
-TOPOS = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 4), (3, 2), (4, 3), (1, 8), (1, 16), (4, 8)]
+TOPOS = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 4), (3, 2), (4, 3), (2, 6), (1, 8), (1, 12), (1, 16),
+         (4, 8)]
 
 
 def run_qgz(g, block, bits, N, M):
