@@ -321,6 +321,8 @@ def run_ours(args):
     copy_gbs = None if args.only else _copy_reference(zpp, torch, dev)
     overlap = None if args.only else _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out,
                                                   per_kernel_bytes)
+    as_tensors = None if args.only else _qgz_tensors(zpp, torch, dev, g, E, c0, s0,
+                                                     per_kernel_bytes)
 
     result = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -330,7 +332,7 @@ def run_ours(args):
               "config": workload_config(div, n_qwz, E),
               "roofline": roof, "kernels": kernels,
               "copy_kernel_gbs": round(copy_gbs, 1) if copy_gbs else None,
-              "qgz_pipelined": overlap,
+              "qgz_pipelined": overlap, "qgz_tensors": as_tensors,
               "gpu_launches": len(active) * args.steps, "clocks": clocks}
     if args.only:
         result["only"] = active[0]
@@ -415,6 +417,44 @@ def _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out, per_kernel_bytes, r
     res["gbs_serial"] = round(qbytes / (res["serial_us"] * 1e-6) / 1e9, 1)
     res["gbs_pipelined"] = round(qbytes / (best * 1e-6) / 1e9, 1)
     return res
+
+
+def _qgz_tensors(zpp, torch, dev, g, E, c0, s0, per_kernel_bytes, reps=20):
+    """K3 on the bucket given as its parameter-gradient tensors (13 per rank): the fused
+    flatten against flattening first (torch.cat into the [W][E] bucket) and then K3."""
+    from quantized_zero_communication_gb300 import inputs
+    N, M = QGZ_N, QGZ_M
+    sizes = inputs.bucket_tensor_sizes()
+    if sum(sizes) != E:  # a reduced workload (--size-div): same tensor count, scaled
+        sizes = [s * E // sum(sizes) // 16 * 16 for s in sizes[:-1]]
+        sizes.append(E - sum(sizes))
+    tensors = inputs.split_bucket(g, sizes)
+    stream = torch.cuda.current_stream(dev)
+
+    def fused():
+        zpp.qgz_reorder_quant_tensors(tensors, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
+
+    def flatten_then_k3():
+        torch.cat(tensors, dim=1, out=g)
+        zpp.qgz_reorder_quant(g, QGZ_BLOCK, QGZ_BITS, N, M, c0, s0)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    us_fused, us_flat = timed(fused), timed(flatten_then_k3)
+    del tensors
+    return {"tensors": len(sizes), "fused_us": round(us_fused, 1),
+            "flatten_then_k3_us": round(us_flat, 1),
+            "fused_gbs": round(per_kernel_bytes["K3_reorder_quant"] / (us_fused * 1e-6) / 1e9, 1)}
 
 
 def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, n_qwz, E,

@@ -90,6 +90,7 @@ typedef struct zpp_local_range {
 #define ZPP_MIN_BLOCK 64
 #define ZPP_MAX_BLOCK 4096
 #define ZPP_MAX_ELEMS (((int64_t)1) << 38)
+#define ZPP_MAX_TENSORS 1024 /* tensors per bucket in zpp_qgz_reorder_quant_tensors */
 
 /*
  * qwZ step 1 -- block-wise symmetric quantisation of a weight shard before the forward
@@ -136,6 +137,27 @@ ZPP_API zpp_status zpp_dequant_blockwise(const void* codes, const float* scales,
 ZPP_API zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
                                  int32_t block, int32_t bits, zpp_topology topo,
                                  void* codes, float* scales, cudaStream_t stream);
+
+/*
+ * qgZ step 1 with the bucket flatten fused in. A rank's gradient bucket is usually the
+ * concatenation of many parameter gradients; this call reads them where they are
+ * instead of from a flattened copy, and writes exactly (bit for bit) what
+ * zpp_qgz_reorder_quant writes for the bucket whose rank r holds, in order, its copies of
+ * tensors 0..num_tensors-1 ([ZeRO++ summary] Approach: slices reordered for correct
+ * placement). The flattening copy -- a full read and write of the bucket -- is saved.
+ *   tensors     : HOST array [num_tensors] of device pointers; tensor t holds the W ranks'
+ *                 copies back to back ([W][sizes[t]] elements of g_dt), 32-byte aligned
+ *   sizes       : HOST array [num_tensors], elements per rank of tensor t: a multiple of
+ *                 16 (else ZPP_ERR_MISALIGNED), 0 allowed (its pointer is then not read)
+ *   num_tensors : 1 .. ZPP_MAX_TENSORS
+ * E = the sum of sizes must satisfy the rules of zpp_qgz_reorder_quant (a multiple of
+ * W*block, E < 2^31); codes and scales are as there. Tensors of one rank may cross slice
+ * and block boundaries freely. Both host arrays are read during the call only.
+ */
+ZPP_API zpp_status zpp_qgz_reorder_quant_tensors(const void* const* tensors, const int64_t* sizes,
+                                                 int32_t num_tensors, zpp_dtype g_dt,
+                                                 int32_t block, int32_t bits, zpp_topology topo,
+                                                 void* codes, float* scales, cudaStream_t stream);
 
 /*
  * qgZ step 2 -- the fused kernel of the intra-node hop: every receiver (n, l)

@@ -157,6 +157,17 @@ def qgz_reorder_quant(grads, dtype: int, block: int, bits: int, N: int, M: int):
     return codes, scales
 
 
+def flatten_bucket(tensors, W: int):
+    """A bucket given as tensors [W][n_t] -> [W][sum n_t]: rank r's bucket is row r of
+    every tensor, in tensor order (the flatten that precedes the gradient exchange)."""
+    return np.concatenate([np.asarray(t).reshape(W, -1) for t in tensors], axis=1)
+
+
+def qgz_reorder_quant_tensors(tensors, dtype: int, block: int, bits: int, N: int, M: int):
+    """Step a3 on a bucket given as tensors: flatten, then qgz_reorder_quant."""
+    return qgz_reorder_quant(flatten_bucket(tensors, N * M), dtype, block, bits, N, M)
+
+
 def dequant_reduce_requant(codes, scales, E: int, block: int, bits: int, N: int, M: int):
     """Hop 1: -> (codes1 uint8 [W][code_bytes(N*S)], scales1 float32 [W][N*S/block])."""
     W = N * M

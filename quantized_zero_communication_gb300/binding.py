@@ -58,6 +58,7 @@ def lib():
         "zpp_dequant_reduce_scaled": [vp, vp, i64, i32, i32, Topology, ctypes.c_float, vp, i32,
                                       vp],
         "zpp_qgz_reorder_quant_range": [vp, i32, i64, i32, i32, Topology, LocalRange, vp, vp, vp],
+        "zpp_qgz_reorder_quant_tensors": [vp, vp, i32, i32, i32, i32, Topology, vp, vp, vp],
         "zpp_dequant_reduce_requant_range": [vp, vp, i64, i32, i32, Topology, LocalRange, vp, vp,
                                              vp],
         "zpp_dequant_reduce_scaled_range": [vp, vp, i64, i32, i32, Topology, LocalRange,
@@ -96,6 +97,16 @@ def zpp_dequant_blockwise(codes, scales, n, block, bits, y, y_dt, stream=0):
 def zpp_qgz_reorder_quant(grads, g_dt, elems_per_rank, block, bits, topo, codes, scales, stream=0):
     return lib().zpp_qgz_reorder_quant(grads, g_dt, elems_per_rank, block, bits, topo, codes,
                                        scales, stream)
+
+
+def zpp_qgz_reorder_quant_tensors(tensor_ptrs, sizes, g_dt, block, bits, topo, codes, scales,
+                                  stream=0):
+    """tensor_ptrs, sizes: Python sequences (marshalled into host arrays for the call)."""
+    T = len(tensor_ptrs)
+    ptrs = (ctypes.c_void_p * max(T, 1))(*tensor_ptrs)
+    lens = (ctypes.c_int64 * max(T, 1))(*sizes)
+    return lib().zpp_qgz_reorder_quant_tensors(ptrs, lens, T, g_dt, block, bits, topo, codes,
+                                               scales, stream)
 
 
 def zpp_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits, topo, out_codes,
@@ -215,6 +226,33 @@ def qgz_reorder_quant(grads, block, bits, N, M, codes=None, scales=None):
     _check(zpp_qgz_reorder_quant(grads.data_ptr(), _dt(grads.dtype), E, block, bits,
                                  Topology(N, M), codes.data_ptr(), scales.data_ptr(),
                                  _stream(grads)), "zpp_qgz_reorder_quant")
+    return codes, scales
+
+
+def qgz_reorder_quant_tensors(tensors, block, bits, N, M, codes=None, scales=None):
+    """The bucket given as a list of gradient tensors, tensor t of shape [W][n_t] (the W
+    ranks' copies; any shape with W * n_t elements, contiguous) -> the codes and scales
+    qgz_reorder_quant gives for the bucket whose rank r concatenates row r of every tensor."""
+    torch = _torch()
+    if not tensors:
+        raise ValueError("qgz_reorder_quant_tensors needs at least one tensor")
+    _cuda(*tensors)
+    W = N * M
+    dt = tensors[0].dtype
+    if any(t.dtype != dt or t.device != tensors[0].device for t in tensors):
+        raise ValueError("all tensors of a bucket share one dtype and device")
+    if any(t.numel() % W for t in tensors):
+        raise ValueError("every tensor holds W equal per-rank copies")
+    sizes = [t.numel() // W for t in tensors]
+    E = sum(sizes)
+    dev = tensors[0].device
+    if codes is None:
+        codes = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty((W, E // block), dtype=torch.float32, device=dev)
+    _check(zpp_qgz_reorder_quant_tensors([t.data_ptr() for t in tensors], sizes, _dt(dt), block,
+                                         bits, Topology(N, M), codes.data_ptr(), scales.data_ptr(),
+                                         _stream(tensors[0])), "zpp_qgz_reorder_quant_tensors")
     return codes, scales
 
 

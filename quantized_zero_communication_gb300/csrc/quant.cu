@@ -16,6 +16,71 @@
 
 namespace zpp {
 
+// Where a warp tile's input elements come from. FlatSrc: one contiguous run that starts at
+// the tile's first element. vec(off) loads the 16 elements at tile offset off (a multiple
+// of 16) as one 256-bit vector; elem(off) loads one element.
+struct FlatSrc {
+  const uint16_t* p;
+  __device__ __forceinline__ U8x32 vec(int off) const { return ld_stream_v8(p + off); }
+  __device__ __forceinline__ uint16_t elem(int off) const { return __ldg(p + off); }
+};
+
+// The fused bucket flatten: rank r's bucket is the concatenation of its copies of the
+// tensors in `tab`, so bucket element i is element i - offs[t] of rank r's copy of tensor
+// t, where offs[t] <= i < offs[t+1]. Tensor t holds the W ranks' copies back to back, rank
+// r's at ptr[t] + r * (offs[t+1] - offs[t]); tensors are multiples of 16 elements, so no
+// 16-element vector straddles two of them.
+struct TensorHit {
+  const uint16_t* ptr;
+  int64_t start, end;  // offs[t], offs[t+1]
+};
+
+// Warp-collective (all 32 lanes, converged): the tensor holding the warp-uniform bucket
+// element a (0 <= a < E). Lanes test 32 candidate ends at once and a ballot counts those
+// <= a (the ends are non-decreasing, so the true ones form a prefix): one round of table
+// loads for up to 32 tensors, two (a coarse pass at stride ceil(T/32) first) for more.
+__device__ __forceinline__ TensorHit find_tensor(const TensorTable& tab, int64_t a, int lane) {
+  const int T = tab.count;
+  int lo = 0;
+  if (T > 32) {
+    const int step = (T + 31) >> 5;
+    lo = __popc(__ballot_sync(~0u, tab.offs[min((lane + 1) * step, T)] <= a)) * step;
+  }
+  const int64_t end = tab.offs[min(lo + lane + 1, T)];
+  const int64_t start = tab.offs[min(lo + lane, T)];
+  const uint16_t* p = tab.ptr[min(lo + lane, T - 1)];
+  const int d = __popc(__ballot_sync(~0u, end <= a));  // tensor lo + d, held by lane d
+  return TensorHit{reinterpret_cast<const uint16_t*>(__shfl_sync(
+                       ~0u, reinterpret_cast<unsigned long long>(p), d)),
+                   __shfl_sync(~0u, start, d), __shfl_sync(~0u, end, d)};
+}
+
+// Input of one warp tile [base, base + extent) of rank r's bucket. When the tile lies in
+// one tensor (all but a handful of tiles), `run` points at its first element and every
+// load is a plain offset; otherwise each load looks its tensor up by binary search.
+struct TensorSrc {
+  const TensorTable& tab;
+  int64_t base;         // bucket index of the tile's first element
+  int64_t r;            // source rank
+  const uint16_t* run;  // rank r's copy of the tile, or null if the tile spans tensors
+  __device__ __forceinline__ const uint16_t* at(int64_t i) const {
+    int lo = 0, hi = tab.count;  // invariant: offs[lo] <= i < offs[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (tab.offs[mid] <= i) lo = mid;
+      else hi = mid;
+    }
+    const int64_t len = tab.offs[lo + 1] - tab.offs[lo];
+    return tab.ptr[lo] + r * len + (i - tab.offs[lo]);
+  }
+  __device__ __forceinline__ U8x32 vec(int off) const {
+    return ld_stream_v8(run ? run + off : at(base + off));
+  }
+  __device__ __forceinline__ uint16_t elem(int off) const {
+    return __ldg(run ? run + off : at(base + off));
+  }
+};
+
 template <int B>
 struct QuantTile {
   static constexpr int VEC = 16;                      // elements per lane per row
@@ -24,13 +89,12 @@ struct QuantTile {
   static constexpr int ROWS = TILE / ROW;
 };
 
-// Quantise one warp tile. `in` points at the tile's first input element, `codes` at its
-// first code byte, `scales` at its first block scale. FULL: all TILE elements valid;
-// otherwise only the first `valid` (any count; lanes past it load zeros, which leave
-// the absmax unchanged and give code 0, and store nothing).
-template <typename TT, int BITS, int B, bool FULL>
-__device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
-                                           uint8_t* __restrict__ codes,
+// Quantise one warp tile. `in` gives the tile's input elements (FlatSrc or TensorSrc),
+// `codes` points at its first code byte, `scales` at its first block scale. FULL: all TILE
+// elements valid; otherwise only the first `valid` (any count; lanes past it load zeros,
+// which leave the absmax unchanged and give code 0, and store nothing).
+template <typename TT, int BITS, int B, bool FULL, typename Src>
+__device__ __forceinline__ void quant_tile(const Src& in, uint8_t* __restrict__ codes,
                                            float* __restrict__ scales, int valid, int lane) {
   using T = QuantTile<B>;
   constexpr int VEC = T::VEC, ROW = T::ROW, ROWS = T::ROWS;
@@ -41,18 +105,18 @@ __device__ __forceinline__ void quant_tile(const uint16_t* __restrict__ in,
     const int off = u * ROW + lane * VEC;
     if (FULL) {
       cnt[u] = VEC;
-      raw[u] = ld_stream_v8(in + off);
+      raw[u] = in.vec(off);
     } else {
       int c = valid - off;
       c = c < 0 ? 0 : (c > VEC ? VEC : c);
       cnt[u] = c;
       if (c == VEC) {
-        raw[u] = ld_stream_v8(in + off);
+        raw[u] = in.vec(off);
       } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) raw[u].w[k] = 0u;
         for (int i = 0; i < c; ++i)
-          raw[u].w[i >> 1] |= static_cast<uint32_t>(__ldg(in + off + i)) << (16 * (i & 1));
+          raw[u].w[i >> 1] |= static_cast<uint32_t>(in.elem(off + i)) << (16 * (i & 1));
       }
     }
   }
@@ -144,10 +208,10 @@ __global__ void __launch_bounds__(kThreads) k_quant(const uint16_t* __restrict__
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
   const int64_t full = n / TILE;
   if (t < full) {
-    quant_tile<TT, BITS, B, true>(x + t * TILE, codes + t * (TILE * BITS / 8),
+    quant_tile<TT, BITS, B, true>(FlatSrc{x + t * TILE}, codes + t * (TILE * BITS / 8),
                                   scales + t * (TILE / B), TILE, lane);
   } else if (t == full && n > full * TILE) {
-    quant_tile<TT, BITS, B, false>(x + t * TILE, codes + t * (TILE * BITS / 8),
+    quant_tile<TT, BITS, B, false>(FlatSrc{x + t * TILE}, codes + t * (TILE * BITS / 8),
                                    scales + t * (TILE / B), static_cast<int>(n - t * TILE), lane);
   }
 }
@@ -173,11 +237,43 @@ __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __re
     const int64_t out_off = r * E + p * S + k * TILE;
     const int64_t rem = S - k * TILE;
     if (rem >= TILE)
-      quant_tile<TT, BITS, B, true>(grads + in_off, codes + out_off * BITS / 8, scales + out_off / B,
-                                    TILE, lane);
+      quant_tile<TT, BITS, B, true>(FlatSrc{grads + in_off}, codes + out_off * BITS / 8,
+                                    scales + out_off / B, TILE, lane);
     else
-      quant_tile<TT, BITS, B, false>(grads + in_off, codes + out_off * BITS / 8,
+      quant_tile<TT, BITS, B, false>(FlatSrc{grads + in_off}, codes + out_off * BITS / 8,
                                      scales + out_off / B, static_cast<int>(rem), lane);
+  }
+}
+
+// K3 with the bucket flatten fused in: as k_reorder_quant (whole exchange), but every
+// rank's bucket is read from its copies of the tensors in `tab` instead of a flat
+// [W][E] buffer. The codes and scales are those of k_reorder_quant over the flattened
+// bucket, bit for bit; the flattening copy (a full read and write of the bucket) is saved.
+template <typename TT, int BITS, int B>
+__global__ void __launch_bounds__(kThreads)
+    k_reorder_quant_tensors(const __grid_constant__ TensorTable tab, int64_t E, int N, int M,
+                            uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  constexpr int TILE = QuantTile<B>::TILE;
+  const int lane = threadIdx.x & 31;
+  const int64_t k = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+  const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
+  const int p = blockIdx.y, r = blockIdx.z;
+  if (k * TILE < S) {
+    const int l_d = p / N, n_d = p - l_d * N;
+    const int64_t j = static_cast<int64_t>(n_d) * M + l_d;
+    const int64_t base = j * S + k * TILE;
+    const int64_t out_off = r * E + p * S + k * TILE;
+    const int64_t rem = S - k * TILE;
+    const TensorHit h = find_tensor(tab, base, lane);  // warp-uniform: k is per warp
+    const bool one = base + (rem < TILE ? rem : TILE) <= h.end;
+    const TensorSrc src{tab, base, r, one ? h.ptr + r * (h.end - h.start) + (base - h.start)
+                                          : nullptr};
+    if (rem >= TILE)
+      quant_tile<TT, BITS, B, true>(src, codes + out_off * BITS / 8, scales + out_off / B, TILE,
+                                    lane);
+    else
+      quant_tile<TT, BITS, B, false>(src, codes + out_off * BITS / 8, scales + out_off / B,
+                                     static_cast<int>(rem), lane);
   }
 }
 
@@ -231,6 +327,19 @@ cudaError_t launch_quant(const void* x, int is_bf16, int64_t n, int block, int b
                          float* scales, cudaStream_t s) {
   return by_type_bits_block(is_bf16, bits, block, [&]<typename TT, int BITS, int B>() {
     return run_quant<TT, BITS, B>(x, n, codes, scales, s);
+  });
+}
+
+cudaError_t launch_reorder_quant_tensors(const TensorTable& tab, int is_bf16, int64_t E, int block,
+                                         int bits, int N, int M, void* codes, float* scales,
+                                         cudaStream_t s) {
+  return by_type_bits_block(is_bf16, bits, block, [&]<typename TT, int BITS, int B>() {
+    const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
+    const int64_t tps = (S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
+    const dim3 grid(tile_grid(tps, kWarps), static_cast<unsigned>(W), static_cast<unsigned>(W));
+    k_reorder_quant_tensors<TT, BITS, B><<<grid, kThreads, 0, s>>>(
+        tab, E, N, M, static_cast<uint8_t*>(codes), scales);
+    return cudaGetLastError();
   });
 }
 

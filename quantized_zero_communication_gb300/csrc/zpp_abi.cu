@@ -134,6 +134,43 @@ zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elem
                                      full_range(topo), codes, scales, stream);
 }
 
+zpp_status zpp_qgz_reorder_quant_tensors(const void* const* tensors, const int64_t* sizes,
+                                         int32_t num_tensors, zpp_dtype g_dt, int32_t block,
+                                         int32_t bits, zpp_topology topo, void* codes,
+                                         float* scales, cudaStream_t stream) {
+  static_assert(zpp::kMaxTensors == ZPP_MAX_TENSORS, "tensor table size");
+  if (!tensors || !sizes || num_tensors < 1 || num_tensors > ZPP_MAX_TENSORS)
+    return ZPP_ERR_INVALID_ARG;
+  int64_t E = 0;
+  for (int32_t t = 0; t < num_tensors; ++t) {
+    if (sizes[t] < 0 || sizes[t] >= (int64_t{1} << 31)) return ZPP_ERR_INVALID_ARG;
+    E += sizes[t];
+    if (E >= (int64_t{1} << 31)) return ZPP_ERR_INVALID_ARG;
+  }
+  int64_t W = 0;
+  zpp_status st = check_topology(E, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (g_dt != ZPP_F16 && g_dt != ZPP_BF16 && g_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (E == 0) return ZPP_OK;
+  if (!codes || !scales) return ZPP_ERR_INVALID_ARG;
+  for (int32_t t = 0; t < num_tensors; ++t)
+    if (sizes[t] > 0 && !tensors[t]) return ZPP_ERR_INVALID_ARG;
+  if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
+  for (int32_t t = 0; t < num_tensors; ++t)
+    if (sizes[t] % 16 != 0 || (sizes[t] > 0 && !aligned(tensors[t], 32))) return ZPP_ERR_MISALIGNED;
+  if (!aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  zpp::TensorTable tab;
+  tab.count = num_tensors;
+  tab.offs[0] = 0;
+  for (int32_t t = 0; t < num_tensors; ++t) {
+    tab.ptr[t] = static_cast<const uint16_t*>(tensors[t]);
+    tab.offs[t + 1] = tab.offs[t] + sizes[t];
+  }
+  return from_cuda(zpp::launch_reorder_quant_tensors(tab, g_dt == ZPP_BF16, E, block, bits,
+                                                     topo.num_nodes, topo.gpus_per_node, codes,
+                                                     scales, stream));
+}
+
 zpp_status zpp_dequant_reduce_requant_range(const void* codes, const float* scales,
                                             int64_t elems_per_rank, int32_t block, int32_t bits,
                                             zpp_topology topo, zpp_local_range range,

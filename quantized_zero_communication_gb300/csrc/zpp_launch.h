@@ -22,6 +22,20 @@ cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int 
                                  int N, int M, int l_begin, int l_end, void* codes, float* scales,
                                  cudaStream_t s);
 
+// K3 over a bucket given as tensors (the flatten fused in; whole exchange only). Tensor t
+// holds the W ranks' copies back to back, rank r's at ptr[t] + r * len_t, len_t =
+// offs[t+1] - offs[t]; offs[0] = 0, offs[count] = E. Passed by value in the kernel's
+// parameter space (about 16 KB), so no device table is needed.
+constexpr int kMaxTensors = 1024;  // = ZPP_MAX_TENSORS
+struct TensorTable {
+  const uint16_t* ptr[kMaxTensors];
+  int64_t offs[kMaxTensors + 1];
+  int32_t count;
+};
+cudaError_t launch_reorder_quant_tensors(const TensorTable& tab, int is_bf16, int64_t E, int block,
+                                         int bits, int N, int M, void* codes, float* scales,
+                                         cudaStream_t s);
+
 // K4: intra-node fused dequantise -> fp32 sum over M chunks -> requantise.
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
                                           int block, int bits, int N, int M, int l_begin,

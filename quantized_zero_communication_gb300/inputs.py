@@ -103,6 +103,42 @@ def gradient_bucket(device="cpu", W=32, elems_per_rank=16_777_216):
     return x.to(torch.bfloat16).reshape(W, elems_per_rank)
 
 
+# The bucket's per-rank content as parameter gradients (for the fused flatten): 4083 rows
+# of a 1024-wide embedding plus one transformer block of hidden 1024 (layer norms, QKV,
+# attention output, a 4x MLP, with biases) -- 13 tensors, 16,777,216 elements per rank.
+BUCKET_TENSOR_SHAPES = (
+    ("embedding_rows", (4083, 1024)), ("ln1_weight", (1024,)), ("ln1_bias", (1024,)),
+    ("qkv_weight", (3072, 1024)), ("qkv_bias", (3072,)), ("out_weight", (1024, 1024)),
+    ("out_bias", (1024,)), ("ln2_weight", (1024,)), ("ln2_bias", (1024,)),
+    ("fc1_weight", (4096, 1024)), ("fc1_bias", (4096,)), ("fc2_weight", (1024, 4096)),
+    ("fc2_bias", (1024,)))
+
+
+def bucket_tensor_sizes():
+    """Elements per rank of each tensor of BUCKET_TENSOR_SHAPES, in order."""
+    return [math.prod(shape) for _, shape in BUCKET_TENSOR_SHAPES]
+
+
+def split_bucket(bucket, sizes):
+    """[W][E] bucket -> one contiguous [W][n_t] tensor per size (consecutive column ranges:
+    the tensors whose per-rank concatenation is the bucket)."""
+    out, at = [], 0
+    for n in sizes:
+        out.append(bucket[:, at:at + n].contiguous())
+        at += n
+    assert at == bucket.shape[1]
+    return out
+
+
+def random_sizes(total, count, seed, unit=16):
+    """`count` sizes, multiples of `unit` (0 allowed), summing to `total` (a multiple of
+    `unit`): seeded uniform cut points."""
+    g = _gen(seed, "cpu")
+    cuts = torch.randint(0, total // unit + 1, (count - 1,), generator=g).sort().values * unit
+    edges = [0] + cuts.tolist() + [total]
+    return [b - a for a, b in zip(edges[:-1], edges[1:])]
+
+
 SWEEP_SIZES = [1 << s for s in range(20, 31, 2)]
 SWEEP_DTYPES = (torch.float16, torch.bfloat16)
 SWEEP_BITS = (8, 4)

@@ -132,6 +132,35 @@ def test_qgz_entry_points_reject_bad_topologies():
 
 
 @cpu_only
+@cpu_only
+def test_tensor_bucket_entry_point_rejects_bad_tables():
+    """zpp_qgz_reorder_quant_tensors: every rule on the tensor list is checked on the host."""
+    topo = zb.Topology(2, 2)  # W = 4; block 128 -> E must be a multiple of 512
+
+    def call(ptrs, sizes, dt=zb.ZPP_BF16, block=128, bits=4, t=topo, codes=FAKE, scales=FAKE):
+        return zb.zpp_qgz_reorder_quant_tensors(ptrs, sizes, dt, block, bits, t, codes, scales)
+
+    INV, MIS, UNS = zb.ZPP_ERR_INVALID_ARG, zb.ZPP_ERR_MISALIGNED, zb.ZPP_ERR_UNSUPPORTED
+    assert zb.lib().zpp_qgz_reorder_quant_tensors(None, None, 1, zb.ZPP_BF16, 128, 4, topo,
+                                                   FAKE, FAKE, None) == INV
+    assert call([], []) == INV                                       # no tensor
+    assert call([FAKE] * 1025, [16] * 1025) == INV                   # over ZPP_MAX_TENSORS
+    assert call([FAKE, FAKE], [528, -16]) == INV                     # negative size
+    assert call([FAKE, FAKE], [256, 240]) == INV                     # E % (W * block) != 0
+    assert call([FAKE], [1 << 31]) == INV                            # E >= 2^31
+    assert call([FAKE, FAKE], [256, 256], t=zb.Topology(0, 2)) == INV
+    assert call([FAKE, FAKE], [256, 256], bits=3) == INV
+    assert call([FAKE, FAKE], [256, 256], dt=7) == INV
+    assert call([FAKE, 0], [256, 256]) == INV                        # null tensor
+    assert call([FAKE, FAKE], [256, 256], codes=0) == INV
+    assert call([FAKE, FAKE], [256, 256], dt=zb.ZPP_F32) == UNS
+    assert call([FAKE, FAKE], [264, 248]) == MIS                     # not a multiple of 16
+    assert call([FAKE, FAKE + 16], [256, 256]) == MIS                # pointer not 32-byte aligned
+    assert call([FAKE, FAKE], [256, 256], codes=FAKE + 16) == MIS
+    assert call([FAKE, FAKE], [256, 256], scales=FAKE + 2) == MIS
+    assert call([0, 0], [0, 0]) == zb.ZPP_OK                         # empty bucket: no launch
+
+
 def test_copy_rejects_bad_sizes():
     assert zb.zpp_device_copy(FAKE, FAKE * 2, 33) == zb.ZPP_ERR_INVALID_ARG
     assert zb.zpp_device_copy(FAKE, FAKE * 2, 0) == zb.ZPP_OK

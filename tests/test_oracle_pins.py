@@ -282,6 +282,31 @@ def test_reorder_is_a_slice_permutation(N, M):
         assert owners == [n * M + l for n in range(N)]
 
 
+@pytest.mark.parametrize("W", [1, 2, 6])
+def test_flatten_bucket_inverts_the_split_into_tensors(W):
+    """The fused flatten's definition: rank r's bucket is row r of every tensor, in tensor
+    order. Cutting a bucket of distinct values (rank r, position i -> r * 10^6 + i) into
+    consecutive column ranges and flattening again must give the bucket back; taking the
+    tensors in another order, or the ranks' rows transposed, must not."""
+    E = 400
+    bucket = (np.arange(W)[:, None] * 10 ** 6 + np.arange(E)[None, :]).astype(np.float64)
+    cuts = [0, 16, 16, 208, 400]  # one empty tensor
+    tensors = [bucket[:, a:b].copy() for a, b in zip(cuts[:-1], cuts[1:])]
+    assert np.array_equal(oracle.flatten_bucket(tensors, W), bucket)
+    assert not np.array_equal(oracle.flatten_bucket(tensors[::-1], W), bucket)
+    if W > 1:
+        flipped = [t.T.copy() for t in tensors]  # [n_t][W]: rank-minor, the wrong layout
+        assert not np.array_equal(oracle.flatten_bucket(flipped, W), bucket)
+
+
+def test_tensor_bucket_with_one_tensor_is_the_flat_call():
+    x = inputs.draw("laplace", 4 * 2048, seed=5, dtype=torch.bfloat16).view(torch.int16).numpy()
+    x = x.view(np.uint16).reshape(4, 2048)
+    a = oracle.qgz_reorder_quant_tensors([x], oracle.BF16, 256, 4, 2, 2)
+    b = oracle.qgz_reorder_quant(x, oracle.BF16, 256, 4, 2, 2)
+    assert all(np.array_equal(u, v) for u, v in zip(a, b))
+
+
 @pytest.mark.parametrize("N,M", [(1, 2), (2, 2), (2, 4), (1, 8), (4, 2)])
 @pytest.mark.parametrize("bits", [4, 8])
 def test_identical_exact_sources_reduce_exactly(N, M, bits):

@@ -197,6 +197,57 @@ def test_qgz_pipeline_topologies(N, M, bits):
             check_qgz(g, block, bits, N, M)
 
 
+# ----------------------------------------------------------------------- fused bucket flatten
+def check_tensor_bucket(g, sizes, block, bits, N, M):
+    """K3 over `g` cut into tensors of `sizes` == the oracle on the flattened tensors == the
+    flat-buffer K3 on `g` (all bit for bit)."""
+    tensors = inputs.split_bucket(g, sizes)
+    c, s = zpp.qgz_reorder_quant_tensors(tensors, block, bits, N, M)
+    oc, os_ = oracle.qgz_reorder_quant_tensors([bits16(t).reshape(t.shape) for t in tensors],
+                                               odt(g.dtype), block, bits, N, M)
+    assert np.array_equal(host(c), oc)
+    assert np.array_equal(host(s).view(np.uint32), os_.view(np.uint32))
+    fc, fs = zpp.qgz_reorder_quant(g, block, bits, N, M)
+    assert torch.equal(c, fc) and torch.equal(s.view(torch.int32), fs.view(torch.int32))
+
+
+@pytest.mark.parametrize("N,M", [(1, 1), (2, 2), (2, 4), (3, 2), (4, 8)])
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_tensor_bucket_equals_flattened_bucket(N, M, bits, dtype):
+    """Tensors of seeded random sizes (multiples of 16, empty ones included) whose edges
+    fall inside blocks, tiles and slices; 1, 5 and 17 tensors."""
+    W = N * M
+    for block, count in ((64, 1), (512, 5), (4096, 17)):
+        per_slice = 3 * 8192 + block if W * W * (3 * 8192 + block) <= (1 << 24) else 2 * block
+        E = W * per_slice
+        g = inputs.draw("laplace", W * E, seed=31 * W + block + bits, dtype=dtype,
+                        device=DEV).reshape(W, E)
+        sizes = inputs.random_sizes(E, count, seed=W + count)
+        check_tensor_bucket(g, sizes, block, bits, N, M)
+
+
+def test_tensor_bucket_largest_table():
+    """ZPP_MAX_TENSORS tensors, many of them one 16-element vector per rank; one more is
+    refused on the host."""
+    N, M, block = 2, 2, 64
+    W = N * M
+    E = W * block * 64  # 16384 elements per rank
+    g = inputs.draw("normal", W * E, seed=77, dtype=torch.bfloat16, device=DEV).reshape(W, E)
+    sizes = inputs.random_sizes(E, 1024, seed=78)
+    check_tensor_bucket(g, sizes, block, 4, N, M)
+    tensors = inputs.split_bucket(g, [16] * 1023 + [E - 16 * 1023 - 16, 16])
+    with pytest.raises(zb.ZppError):
+        zpp.qgz_reorder_quant_tensors(tensors, block, 4, N, M)
+
+
+def test_tensor_bucket_rejects_unaligned_sizes():
+    g = torch.zeros((4, 1024), dtype=torch.float16, device=DEV)
+    with pytest.raises(zb.ZppError) as e:
+        zpp.qgz_reorder_quant_tensors(inputs.split_bucket(g, [24, 1000]), 64, 4, 2, 2)
+    assert e.value.status == zb.ZPP_ERR_MISALIGNED
+
+
 @pytest.mark.parametrize("N,M", [(2, 4), (3, 2), (4, 8)])
 @pytest.mark.parametrize("bits", [4, 8])
 def test_averaged_owner_slices(N, M, bits):
@@ -319,6 +370,14 @@ def test_gradient_bucket_full_size():
     """qgZ on a 536,870,912-element bf16 bucket over 4 nodes x 8 GPUs, INT4 block 512."""
     g = inputs.gradient_bucket(DEV)
     check_qgz(g, 512, 4, 4, 8)
+
+
+@pytest.mark.slow
+def test_gradient_bucket_as_tensors_full_size():
+    """The 4 x 8 bucket given as its 13 parameter-gradient tensors per rank: the fused
+    flatten equals the oracle on the flattened bucket and the flat-buffer K3."""
+    g = inputs.gradient_bucket(DEV)
+    check_tensor_bucket(g, inputs.bucket_tensor_sizes(), 512, 4, 4, 8)
 
 
 @pytest.mark.slow
