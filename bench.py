@@ -67,6 +67,13 @@ def step_bytes(n_qwz, E, div=1):
     return b
 
 
+def step_elements(n_qwz, E):
+    """Input elements per launch of each kernel (for elements/s)."""
+    W, M = QGZ_N * QGZ_M, QGZ_M
+    return {"K1_quant": n_qwz, "K2_dequant": n_qwz, "K3_reorder_quant": W * E,
+            "K4_dequant_reduce_requant": W * E, "K5_dequant_reduce": W * (E // M)}
+
+
 def workload_sizes(div):
     from quantized_zero_communication_gb300 import inputs
     return inputs.GPT_LAYER_ELEMS // div, QGZ_ELEMS_PER_RANK // div
@@ -310,6 +317,7 @@ def run_ours(args):
         gbs = per_kernel_bytes[k] / avg_s / 1e9
         kernels[k] = {"us": round(avg_s * 1e6, 2), "bytes": per_kernel_bytes[k],
                       "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                      "gelem_per_s": round(step_elements(n_qwz, E)[k] / avg_s / 1e9, 1),
                       "share": round(kt[k] / sum(kt.values()), 4)}
     dom = max(active, key=lambda k: kt[k])
     full_bytes = step_bytes(*workload_sizes(1))[dom]
@@ -319,6 +327,9 @@ def run_ours(args):
             "traffic": ncu_traffic(dom, per_kernel_bytes[dom] / full_bytes)}
     # same-run copy kernel on 1 GiB (reference for the same HBM)
     copy_gbs = None if args.only else _copy_reference(zpp, torch, dev)
+    if copy_gbs:
+        for k in active:
+            kernels[k]["frac_same_run_copy"] = round(kernels[k]["gbs"] / copy_gbs, 4)
     overlap = None if args.only else _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out,
                                                   per_kernel_bytes)
     as_tensors = None if args.only else _qgz_tensors(zpp, torch, dev, g, E, c0, s0,
