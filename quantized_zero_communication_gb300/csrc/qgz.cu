@@ -224,22 +224,26 @@ __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
                                      out_scales);
 }
 
-// K4, INT4, exactly KC (2, 4 or 8) sources per receiver, full CTA tiles only: every thread
+template <int KC>
+constexpr int staged_smem_bytes() { return KC * kThreads * 16; }
+
+// K4, INT4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every thread
 // stages its 16 code bytes of each source in shared memory with cp.async (the copies do not
 // occupy registers, so 4 CTAs fit per SM), in two commit groups; the first half of the
 // sources is reduced while the second half is still landing. Each thread reads back only
 // the slots it filled, and every slot is written once per launch, so no barrier is needed.
 // Measured on GB300 (4 x 8 bucket) 68 us against 72 us for the same tile with the codes
-// held in registers at 3 CTAs per SM.
+// held in registers at 3 CTAs per SM. With 16 sources the stage is 64 KB (3 CTAs per SM).
 template <int KC, int SPLIT>
-__global__ void __launch_bounds__(kThreads, kStagedMinCtas)
+__global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
     k_dequant_reduce_requant_staged(const uint8_t* __restrict__ codes,
                                     const float* __restrict__ scales, int64_t E, int log2b,
                                     int l_begin, uint8_t* __restrict__ out_codes,
                                     float* __restrict__ out_scales) {
   using G = Geo4<4>;
   constexpr int M = KC, H = KC / 2;
-  __shared__ uint4 stage[KC][kThreads];
+  extern __shared__ uint4 stage_mem[];  // [KC][kThreads], staged_smem_bytes<KC>()
+  uint4(*stage)[kThreads] = reinterpret_cast<uint4(*)[kThreads]>(stage_mem);
   __shared__ float red[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
@@ -309,6 +313,22 @@ __global__ void __launch_bounds__(kThreads)
 
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
 
+template <int KC, int SPLIT>
+static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, int log2b, int lb,
+                              int64_t full, unsigned ny, unsigned nz, uint8_t* oc,
+                              float* out_scales, cudaStream_t s) {
+  constexpr int smem = staged_smem_bytes<KC>();
+  auto kern = k_dequant_reduce_requant_staged<KC, SPLIT>;
+  if constexpr (smem > 48 * 1024) {  // above the default dynamic shared-memory limit
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<dim3(static_cast<unsigned>(full), ny, nz), kThreads, smem, s>>>(c, scales, E, log2b, lb,
+                                                                        oc, out_scales);
+  return cudaGetLastError();
+}
+
 template <int BITS, int KC>
 static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int log2b, int N,
                            int M, int lb, int le, void* out_codes, float* out_scales,
@@ -319,13 +339,15 @@ static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, in
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
   const unsigned ny = static_cast<unsigned>(le - lb), nz = static_cast<unsigned>(N);
   if constexpr (BITS == 4 && KC >= 2) {
-    if (M == KC) {  // one chunk of sources: staged kernel on the full tiles, then the tail
-      constexpr int SPLIT = KC >= 4 ? kSplitWords : 0;
+    if (M == KC || (KC == 8 && M == 16)) {  // one stage of sources on the full tiles, then the tail
       const int64_t full = C / CTA;
+      cudaError_t err = cudaSuccess;
       if (full > 0)
-        k_dequant_reduce_requant_staged<KC, SPLIT><<<dim3(static_cast<unsigned>(full), ny, nz),
-                                                     kThreads, 0, s>>>(c, scales, E, log2b, lb, oc,
-                                                                       out_scales);
+        err = M == 16 ? run_staged<16, kSplitWords>(c, scales, E, log2b, lb, full, ny, nz, oc,
+                                                    out_scales, s)
+                      : run_staged<KC, KC >= 4 ? kSplitWords : 0>(c, scales, E, log2b, lb, full,
+                                                                  ny, nz, oc, out_scales, s);
+      if (err != cudaSuccess) return err;
       if (C % CTA != 0) {
         if constexpr (KC >= 4)
           k_dequant_reduce_requant_split<KC><<<dim3(1, ny, nz), kThreads, 0, s>>>(
