@@ -25,15 +25,22 @@ namespace zpp {
 
 // Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
 // in K5; a CTA tile is 8 warps x one row.
-// K4 with INT4 codes and M a multiple of a chunk of 4 or 8 sources runs as
-// k_dequant_reduce_requant_split: kSplitWords of the 4 code words per source are converted
-// by int4x8_to_f2_eo (which shares the conversion between the integer and fp32 pipes),
-// under a register budget of kSplitMinCtas CTAs of 256 threads per SM. Measured on GB300
-// (4 x 8 bucket, K = 8) this pair is the fastest; with 2 sources per chunk the kernel is
-// nearer its memory bound and the plain conversion is faster.
+//
+// K4 kernels, chosen per launch by run_drr (all give the same bits):
+//   k_dequant_reduce_requant_staged<KC, SPLIT>  INT4, M = KC in {2, 4, 8} or M = 16: the
+//       full CTA tiles, the sources' codes staged in shared memory by cp.async;
+//   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
+//       chunk otherwise, and the ragged last tile of a staged launch;
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else (INT8, M not a multiple of
+//       its chunk, 1 or 2 sources per chunk).
+// With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
+// int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
+// on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
+// per SM for the register-held split kernel, 4 for the staged one); with 2 sources per
+// chunk the plain conversion is faster.
 constexpr int kSplitWords = 3;
-constexpr int kSplitMinCtas = 3;
-constexpr int kStagedMinCtas = 4;  // k_dequant_reduce_requant_staged: 64 registers, 32 KB smem
+constexpr int kSplitMinCtas = 3;   // k_dequant_reduce_requant_split: 80 registers
+constexpr int kStagedMinCtas = 4;  // k_dequant_reduce_requant_staged (KC <= 8): 64 registers
 
 template <int BITS>
 struct Geo4 {
@@ -227,10 +234,10 @@ __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
 template <int KC>
 constexpr int staged_smem_bytes() { return KC * kThreads * 16; }
 
-// K4, INT4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every thread
-// stages its 16 code bytes of each source in shared memory with cp.async (the copies do not
-// occupy registers, so 4 CTAs fit per SM), in two commit groups; the first half of the
-// sources is reduced while the second half is still landing. Each thread reads back only
+// K4, INT4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every
+// thread stages its 16 code bytes of each source in shared memory with cp.async (the copies
+// do not occupy registers, so 4 CTAs fit per SM), in two commit groups; the first half of
+// the sources is reduced while the second half is still landing. Each thread reads back only
 // the slots it filled, and every slot is written once per launch, so no barrier is needed.
 // Measured on GB300 (4 x 8 bucket) 68 us against 72 us for the same tile with the codes
 // held in registers at 3 CTAs per SM. With 16 sources the stage is 64 KB (3 CTAs per SM).
@@ -274,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     accumulate<4, 4, SPLIT>(acc, w, s[i]);
   }
-  requant_store<4, SPLIT>(acc, lane, warp, 1 << log2b, e, true, r * (C / 2),
-                                r * (C >> log2b), out_codes, out_scales, red);
+  requant_store<4, SPLIT>(acc, lane, warp, 1 << log2b, e, true, r * (C / 2), r * (C >> log2b),
+                          out_codes, out_scales, red);
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
