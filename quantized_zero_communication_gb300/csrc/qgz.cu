@@ -31,8 +31,8 @@ namespace zpp {
 //       full CTA tiles, the sources' codes staged in shared memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else (INT8, M not a multiple of
-//       its chunk, 1 or 2 sources per chunk).
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else: INT8, M = 1, M not a
+//       multiple of its chunk, and the ragged last tile of a 2-source staged launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
