@@ -27,12 +27,13 @@ namespace zpp {
 // in K5; a CTA tile is 8 warps x one row.
 //
 // K4 kernels, chosen per launch by run_drr (all give the same bits):
-//   k_dequant_reduce_requant_staged<KC, SPLIT>  INT4, M = KC in {2, 4, 8} or M = 16: the
+//   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  M = KC in {2, 4, 8} or M = 16: the
 //       full CTA tiles, the sources' codes staged in shared memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else: INT8, M = 1, M not a
-//       multiple of its chunk, and the ragged last tile of a 2-source staged launch.
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else: M = 1, M not a multiple
+//       of its chunk, INT8 M a multiple of 8 above 16, and the ragged last tile of an INT8
+//       or a 2-source staged launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
@@ -234,20 +235,20 @@ __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
 template <int KC>
 constexpr int staged_smem_bytes() { return KC * kThreads * 16; }
 
-// K4, INT4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every
-// thread stages its 16 code bytes of each source in shared memory with cp.async (the copies
-// do not occupy registers, so 4 CTAs fit per SM), in two commit groups; the first half of
-// the sources is reduced while the second half is still landing. Each thread reads back only
+// K4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every thread
+// stages its 16 code bytes of each source (32 INT4 or 16 INT8 codes) in shared memory with
+// cp.async (the copies do not occupy registers, so 4 CTAs fit per SM), in two commit
+// groups; the first half of the sources is reduced while the second half is still landing. Each thread reads back only
 // the slots it filled, and every slot is written once per launch, so no barrier is needed.
 // Measured on GB300 (4 x 8 bucket) 68 us against 72 us for the same tile with the codes
 // held in registers at 3 CTAs per SM. With 16 sources the stage is 64 KB (3 CTAs per SM).
-template <int KC, int SPLIT>
+template <int BITS, int KC, int SPLIT>
 __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
     k_dequant_reduce_requant_staged(const uint8_t* __restrict__ codes,
                                     const float* __restrict__ scales, int64_t E, int log2b,
                                     int l_begin, uint8_t* __restrict__ out_codes,
                                     float* __restrict__ out_scales) {
-  using G = Geo4<4>;
+  using G = Geo4<BITS>;
   constexpr int M = KC, H = KC / 2;
   extern __shared__ uint4 stage_mem[];  // [KC][kThreads], staged_smem_bytes<KC>()
   uint4(*stage)[kThreads] = reinterpret_cast<uint4(*)[kThreads]>(stage_mem);
@@ -256,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
   const int64_t C = E / M;
-  const int64_t cb_in = E / 2, sc_in = E >> log2b;
+  const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
   const int64_t e = static_cast<int64_t>(blockIdx.x) * G::CTA + warp * G::ROW + lane * G::EPL;
   const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
-  const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx / 2;
+  const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx * BITS / 8;
   const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
 #pragma unroll
   for (int i = 0; i < KC; ++i) {
@@ -279,10 +280,10 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
     if (i == H) cp_async_wait<0>();
     const uint4 v = stage[i][threadIdx.x];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    accumulate<4, 4, SPLIT>(acc, w, s[i]);
+    accumulate<BITS, 4, SPLIT>(acc, w, s[i]);
   }
-  requant_store<4, SPLIT>(acc, lane, warp, 1 << log2b, e, true, r * (C / 2), r * (C >> log2b),
-                          out_codes, out_scales, red);
+  requant_store<BITS, SPLIT>(acc, lane, warp, 1 << log2b, e, true, r * (C * BITS / 8),
+                             r * (C >> log2b), out_codes, out_scales, red);
 }
 
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
@@ -320,12 +321,12 @@ __global__ void __launch_bounds__(kThreads)
 
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
 
-template <int KC, int SPLIT>
+template <int BITS, int KC, int SPLIT>
 static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, int log2b, int lb,
                               int64_t full, unsigned ny, unsigned nz, uint8_t* oc,
                               float* out_scales, cudaStream_t s) {
   constexpr int smem = staged_smem_bytes<KC>();
-  auto kern = k_dequant_reduce_requant_staged<KC, SPLIT>;
+  auto kern = k_dequant_reduce_requant_staged<BITS, KC, SPLIT>;
   if constexpr (smem > 48 * 1024) {  // above the default dynamic shared-memory limit
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                smem);
@@ -345,18 +346,22 @@ static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, in
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
   const unsigned ny = static_cast<unsigned>(le - lb), nz = static_cast<unsigned>(N);
-  if constexpr (BITS == 4 && KC >= 2) {
+  if constexpr (KC >= 2) {
     if (M == KC || (KC == 8 && M == 16)) {  // one stage of sources on the full tiles, then the tail
+      constexpr int SPLIT = BITS == 4 && KC >= 4 ? kSplitWords : 0;
       const int64_t full = C / CTA;
       cudaError_t err = cudaSuccess;
-      if (full > 0)
-        err = M == 16 ? run_staged<16, kSplitWords>(c, scales, E, log2b, lb, full, ny, nz, oc,
-                                                    out_scales, s)
-                      : run_staged<KC, KC >= 4 ? kSplitWords : 0>(c, scales, E, log2b, lb, full,
-                                                                  ny, nz, oc, out_scales, s);
+      if (full > 0) {
+        if (M == KC)
+          err = run_staged<BITS, KC, SPLIT>(c, scales, E, log2b, lb, full, ny, nz, oc, out_scales,
+                                            s);
+        else if constexpr (KC == 8)  // M == 16
+          err = run_staged<BITS, 16, SPLIT>(c, scales, E, log2b, lb, full, ny, nz, oc, out_scales,
+                                            s);
+      }
       if (err != cudaSuccess) return err;
       if (C % CTA != 0) {
-        if constexpr (KC >= 4)
+        if constexpr (BITS == 4 && KC >= 4)
           k_dequant_reduce_requant_split<KC><<<dim3(1, ny, nz), kThreads, 0, s>>>(
               c, scales, E, log2b, M, lb, static_cast<int>(full), oc, out_scales);
         else
