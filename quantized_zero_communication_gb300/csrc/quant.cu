@@ -55,14 +55,12 @@ __device__ __forceinline__ TensorHit find_tensor(const TensorTable& tab, int64_t
                    __shfl_sync(~0u, start, d), __shfl_sync(~0u, end, d)};
 }
 
-// Input of one warp tile [base, base + extent) of rank r's bucket. When the tile lies in
-// one tensor (all but a handful of tiles), `run` points at its first element and every
-// load is a plain offset; otherwise each load looks its tensor up by binary search.
+// Input of a warp tile of rank r's bucket that spans several tensors (a tile inside one
+// tensor is read as a FlatSrc run): each load looks its tensor up by binary search.
 struct TensorSrc {
   const TensorTable& tab;
-  int64_t base;         // bucket index of the tile's first element
-  int64_t r;            // source rank
-  const uint16_t* run;  // rank r's copy of the tile, or null if the tile spans tensors
+  int64_t base;  // bucket index of the tile's first element
+  int64_t r;     // source rank
   __device__ __forceinline__ const uint16_t* at(int64_t i) const {
     int lo = 0, hi = tab.count;  // invariant: offs[lo] <= i < offs[hi]
     while (hi - lo > 1) {
@@ -73,12 +71,8 @@ struct TensorSrc {
     const int64_t len = tab.offs[lo + 1] - tab.offs[lo];
     return tab.ptr[lo] + r * len + (i - tab.offs[lo]);
   }
-  __device__ __forceinline__ U8x32 vec(int off) const {
-    return ld_stream_v8(run ? run + off : at(base + off));
-  }
-  __device__ __forceinline__ uint16_t elem(int off) const {
-    return __ldg(run ? run + off : at(base + off));
-  }
+  __device__ __forceinline__ U8x32 vec(int off) const { return ld_stream_v8(at(base + off)); }
+  __device__ __forceinline__ uint16_t elem(int off) const { return __ldg(at(base + off)); }
 };
 
 template <int B>
@@ -265,15 +259,17 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t out_off = r * E + p * S + k * TILE;
     const int64_t rem = S - k * TILE;
     const TensorHit h = find_tensor(tab, base, lane);  // warp-uniform: k is per warp
-    const bool one = base + (rem < TILE ? rem : TILE) <= h.end;
-    const TensorSrc src{tab, base, r, one ? h.ptr + r * (h.end - h.start) + (base - h.start)
-                                          : nullptr};
-    if (rem >= TILE)
-      quant_tile<TT, BITS, B, true>(src, codes + out_off * BITS / 8, scales + out_off / B, TILE,
-                                    lane);
-    else
-      quant_tile<TT, BITS, B, false>(src, codes + out_off * BITS / 8, scales + out_off / B,
-                                     static_cast<int>(rem), lane);
+    uint8_t* c = codes + out_off * BITS / 8;
+    float* sc = scales + out_off / B;
+    if (base + (rem < TILE ? rem : TILE) <= h.end) {  // the tile lies in one tensor
+      const FlatSrc src{h.ptr + r * (h.end - h.start) + (base - h.start)};
+      if (rem >= TILE) quant_tile<TT, BITS, B, true>(src, c, sc, TILE, lane);
+      else quant_tile<TT, BITS, B, false>(src, c, sc, static_cast<int>(rem), lane);
+    } else {
+      const TensorSrc src{tab, base, r};
+      if (rem >= TILE) quant_tile<TT, BITS, B, true>(src, c, sc, TILE, lane);
+      else quant_tile<TT, BITS, B, false>(src, c, sc, static_cast<int>(rem), lane);
+    }
   }
 }
 
