@@ -2,7 +2,8 @@
  * check codes, scales and the dequantised values, then exercise the error paths.
  * Expected values: tests/golden/quant_tiny.txt, case int4_ties, each 4-element block
  * embedded at the start of a 64-element block of zeros (zeros leave absmax, scale and
- * codes unchanged). Exit status 0 on success. */
+ * codes unchanged). Then qgZ step 1 on the same data, flat and as a list of two tensors.
+ * Exit status 0 on success. */
 #include <stdio.h>
 #include <string.h>
 #include <cuda_runtime_api.h>
@@ -57,6 +58,37 @@ int main(void) {
     CHECK(scales[b] == want_scale[b], "scales");
     for (int i = 0; i < 4; ++i) CHECK(y[b * B + i] == want_y[b][i], "dequantised values");
     for (int i = 4; i < B; ++i) CHECK(y[b * B + i] == 0.0f, "zero padding");
+  }
+
+  /* qgZ step 1 on one rank (topology 1 x 1), once on the flat buffer and once with the same
+   * 128 elements given as two tensors of 64 (host arrays of device pointers and sizes):
+   * the outputs must be identical. */
+  {
+    const zpp_topology one = {1, 1};
+    void *dc1 = NULL, *dc2 = NULL;
+    float *ds1 = NULL, *ds2 = NULL;
+    CHECK(cudaMalloc(&dc1, N / 2) == cudaSuccess && cudaMalloc(&dc2, N / 2) == cudaSuccess, "cudaMalloc c");
+    CHECK(cudaMalloc((void**)&ds1, NB * sizeof(float)) == cudaSuccess, "cudaMalloc s1");
+    CHECK(cudaMalloc((void**)&ds2, NB * sizeof(float)) == cudaSuccess, "cudaMalloc s2");
+    const void* tensors[2] = {dx, (const char*)dx + B * sizeof(unsigned short)};
+    const int64_t sizes[2] = {B, B};
+    CHECK(zpp_qgz_reorder_quant(dx, ZPP_F16, N, B, 4, one, dc1, ds1, 0) == ZPP_OK, "flat step 1");
+    CHECK(zpp_qgz_reorder_quant_tensors(tensors, sizes, 2, ZPP_F16, B, 4, one, dc2, ds2, 0) == ZPP_OK,
+          "tensor-list step 1");
+    unsigned char c1[N / 2], c2[N / 2];
+    float s1[NB], s2[NB];
+    CHECK(cudaMemcpy(c1, dc1, sizeof c1, cudaMemcpyDeviceToHost) == cudaSuccess, "copy c1");
+    CHECK(cudaMemcpy(c2, dc2, sizeof c2, cudaMemcpyDeviceToHost) == cudaSuccess, "copy c2");
+    CHECK(cudaMemcpy(s1, ds1, sizeof s1, cudaMemcpyDeviceToHost) == cudaSuccess, "copy s1");
+    CHECK(cudaMemcpy(s2, ds2, sizeof s2, cudaMemcpyDeviceToHost) == cudaSuccess, "copy s2");
+    CHECK(memcmp(c1, c2, sizeof c1) == 0 && memcmp(s1, s2, sizeof s1) == 0, "tensor list == flat");
+    const int64_t odd[2] = {B + 8, B - 8};
+    CHECK(zpp_qgz_reorder_quant_tensors(tensors, odd, 2, ZPP_F16, B, 4, one, dc2, ds2, 0) ==
+              ZPP_ERR_MISALIGNED, "tensor sizes must be multiples of 16");
+    cudaFree(dc1);
+    cudaFree(dc2);
+    cudaFree(ds1);
+    cudaFree(ds2);
   }
 
   /* rejected before any launch; nothing written */
