@@ -641,8 +641,8 @@ def run_reference(args):
 def run_sweep(args):
     """Times K1, K2 and the fused K-way hop (topology 1 x K, K in {2, 8, 16}) over the
     sweep's sizes x dtypes x bits x blocks (N(0, 0.02) data; timing does not depend on the
-    values), 20 event-timed launches each after 3 warm-up ones, L2 larger than nothing:
-    sizes below the 129 MB L2 are flushed by a 256 MiB write between launches."""
+    values), 20 event-timed launches each after 3 warm-up ones; sizes whose buffers fit in
+    the 129 MB L2 are flushed by a 256 MiB write between launches."""
     import torch
     import quantized_zero_communication_gb300 as zpp
     from quantized_zero_communication_gb300 import build as zbuild, inputs
