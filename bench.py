@@ -600,8 +600,15 @@ def cpu_baseline(target_s):
     what = "the whole workload" if div == 1 else (
         f"1/{div} of the workload (first 1/{div} of the layer weights; bucket with "
         f"{QGZ_ELEMS_PER_RANK // div} elements per rank, same topology)")
+    # the same oracle on one core, over a smaller sample (about a fifth of the time)
+    oracle.set_threads(1)
+    div1, _ = _calibrated_div(max(target_s / 5, 0.5))
+    b1, t1 = oracle_sample_step(div1)
+    oracle.set_threads(cores)
     return {"value": round(tot_b / tot_t / 1e9, 3), "unit": UNIT, "cores": cores,
-            "kind": "oracle", "sample": f"{what}, {reps} pass(es), {tot_t:.1f} s"}
+            "kind": "oracle", "sample": f"{what}, {reps} pass(es), {tot_t:.1f} s",
+            "single_core": {"value": round(b1 / t1 / 1e9, 3), "unit": UNIT,
+                            "sample": f"1/{div1} of the workload, {t1:.1f} s"}}
 
 
 def run_reference(args):
