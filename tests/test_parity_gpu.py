@@ -162,7 +162,7 @@ def test_qwz_round_trip_workload():
 
 # ----------------------------------------------------------------------- qgZ (K3, K4, K5)
 TOPOS = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 4), (3, 2), (4, 3), (2, 6), (1, 8), (1, 12), (1, 16),
-         (2, 16), (1, 32), (4, 8)]
+         (2, 16), (1, 32), (8, 2), (16, 1), (4, 8)]
 
 
 def run_qgz(g, block, bits, N, M):
