@@ -365,12 +365,13 @@ def _two_hop_bound(xs, N, M, block, bits):
     return bounds
 
 
-def test_two_hop_result_matches_direct_sum_within_two_quantisations():
+@pytest.mark.parametrize("N,M,bits", [(2, 4, 4), (2, 4, 8), (4, 2, 4), (4, 2, 8)])
+def test_two_hop_result_matches_direct_sum_within_two_quantisations(N, M, bits):
     """Approach: dequantise before reducing; LIT-102 Key takeaways: reduce locally in
-    higher precision, a fixed number of quantisations per value. On the qgZ tiny topology
-    (2 nodes x 4 GPUs, B=128, INT4) every owner element is within the bound of the two
-    quantisation steps of the direct sum over all ranks."""
-    N, M, B, bits = 2, 4, 128, 4
+    higher precision, a fixed number of quantisations per value. On the qgZ tiny workload
+    (8 ranks, B=128; as 2 nodes x 4 GPUs and as 4 x 2, INT4 and INT8) every owner element
+    is within the bound of the two quantisation steps of the direct sum over all ranks."""
+    B = 128
     g = inputs.qgz_tiny()
     W, E = g.shape
     S = E // W
