@@ -460,6 +460,26 @@ def test_average_of_identical_exact_sources_is_the_own_slice(N, M):
     assert np.array_equal(avg16, bits16(torch.from_numpy(row).to(torch.bfloat16)).reshape(W, S))
 
 
+def test_averaged_two_hop_with_an_inexact_average_within_bound():
+    """W = 6 (3 nodes x 2 GPUs): 1/W is not a power of two, so post_scale = fp32(1/6) carries
+    one rounding (<= u relative) on top of the product's own (<= u): the averaged owner
+    slices stay within the two-quantisation bound / W of the direct average plus 2u."""
+    N, M, B, bits = 3, 2, 128, 4
+    W = N * M
+    E = W * B * 8
+    g = inputs.draw("laplace", W * E, seed=61, dtype=torch.bfloat16).reshape(W, E)
+    S = E // W
+    xs = g.double().numpy()
+    c0, s0, c1, s1, total = oracle.qgz_pipeline(bits16(g), oracle.BF16, B, bits, N, M)
+    direct = np.stack([xs[:, r * S:(r + 1) * S].sum(0) for r in range(W)]) / W
+    bound = _two_hop_bound(xs, N, M, B, bits) / W
+    ps = float(np.float32(1.0 / W))
+    avg = oracle.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, ps, oracle.F32).astype(np.float64)
+    assert np.all(np.abs(avg - direct) <= bound + 2 * U * np.abs(avg) + 1e-30)
+    # the average is the sum times fp32(1/W), rounded once: exactly fp32(total * ps)
+    assert np.array_equal(avg.astype(np.float32), (total.astype(np.float64) * ps).astype(np.float32))
+
+
 def test_averaged_two_hop_result_within_bound():
     """The averaged (1/W) owner slices of the 2 x 4 workload stay within the two-quantisation
     bound of the direct average, in fp32 and after a bf16 cast (plus half a bf16 ulp)."""
