@@ -1,7 +1,9 @@
 """Compile the CPU oracle (test infrastructure) into ``oracle/liboracle.so``.
 
-The flags keep every fp32 operation separately rounded: no FMA contraction, no
-fast-math, IEEE division. OpenMP only parallelises independent blocks and receivers.
+The flags keep the compiler from fusing or reordering anything: no FMA contraction, no
+fast-math, IEEE division. The only fused operations are the ones the source spells out
+(the exact quantiser product in double, and fmaf for each term of the hop sums).
+OpenMP only parallelises independent blocks and receivers.
 """
 import os
 import subprocess

@@ -437,6 +437,40 @@ def test_golden_qgz_fused_sum():
     check_qgz_case(case, *res)
 
 
+def test_fixtures_exclude_the_separately_rounded_reading():
+    """The two fused roundings of the oracle (the quantiser's exact product, one rounding
+    per hop term) against the alternative that rounds every product to fp32 first. Both
+    hand-derived fixtures are cases where the two readings differ: the alternative, redone
+    here with numpy's IEEE fp32 operations, gives the excluded values the fixtures record
+    (code 64, sum bits 0x3fa49249), and the oracle does not."""
+    f32 = np.float32
+    # int8_exact_product_tie: x = 1.5 in a block with amax 3.
+    inv = f32(127) / f32(3)
+    two_step = np.rint(f32(1.5) * inv)                     # the fp32 product is exactly 63.5
+    assert f32(1.5) * inv == f32(63.5) and two_step == 64.0
+    case = {c["name"]: c for c in load_quant_cases()}["int8_exact_product_tie"]
+    xt = torch.tensor(case["x"], dtype=torch.float64).to(torch.float16)
+    codes, _ = oracle.quant_blockwise(bits16(xt), oracle.F16, case["block"], case["bits"])
+    got = unpack_codes(codes, len(case["x"]), 8)
+    assert got[1] == 63 and got[1] != two_step and got[2] == -63
+    # qgz_fused_sum: hop-1 element 0 is 2 s + 7 s with s = fl32(1/7).
+    s = f32(1) / f32(7)
+    separate = f32(f32(2) * s) + f32(f32(7) * s)           # two roundings of the second term
+    assert separate.view(np.uint32) == 0x3fa49249
+    fused = f32(float(s) * 9.0)                             # 2 s + 7 s is exact in double
+    assert fused.view(np.uint32) == 0x3fa4924a
+    qcase = load_qgz_case()
+    g = qgz_case_inputs(qcase)
+    dt = oracle.F16 if qcase["dtype"] == "f16" else oracle.BF16
+    s1 = oracle.qgz_pipeline(bits16(g), dt, qcase["block"], qcase["bits"], qcase["N"],
+                             qcase["M"])[3]
+    # the hop-1 block scale is fl32(sum / 7): 0x3e3c14e7 from the fused sum, 0x3e3c14e6
+    # from the separately rounded one
+    got = np.asarray(s1)[0, 0:1].view(np.uint32)[0]
+    assert (fused / f32(7)).view(np.uint32) == got == 0x3e3c14e7
+    assert (separate / f32(7)).view(np.uint32) == 0x3e3c14e6
+
+
 @pytest.mark.parametrize("N,M", [(2, 2), (2, 4), (1, 8)])
 def test_average_of_identical_exact_sources_is_the_own_slice(N, M):
     """The abstract describes the gradient step as an average: with every rank holding the

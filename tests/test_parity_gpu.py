@@ -1,7 +1,8 @@
 """GPU parity: every kernel, called through the C ABI, against the CPU oracle on the same
 seeded inputs. Codes, scales, dequantised fp16/bf16 values and the reorder permutation
-must match bit for bit; fp32 sums (fixed ascending order, no FMA) are required within
-1e-6 relative and are expected to match exactly, which is also checked.
+must match bit for bit; fp32 sums (fixed ascending order, each term added with one
+rounding as a fused multiply-add) are required within 1e-6 relative and are expected to
+match exactly, which is also checked.
 
 Sizes span several warp tiles plus a ragged tail, every block size and both code widths,
 the small and the full-size workloads, and the edge cases (empty, one element, odd
