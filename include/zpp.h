@@ -238,6 +238,27 @@ ZPP_API int64_t zpp_num_scales(int64_t n, int32_t block);
 ZPP_API const char* zpp_status_string(zpp_status status);
 
 /*
+ * Fault word of the current device (no counterpart in the pages). Kernels that wait for
+ * data in flight (the INT8 fused-hop kernel waits on shared-memory barriers completed by
+ * bulk copies) bound every wait to about a second; a wait that runs out sets a bit here,
+ * the kernel still ends, and its outputs are unspecified. Bits: 1 and 2 -- a wait of the
+ * INT8 fused hop ran out; 4 -- zpp_wait_selftest ran out (as it always does).
+ *   flags : out, the word (0 when nothing ran out since the last clear)
+ *   clear : nonzero -> zero the word after reading it
+ * Unlike the other calls this one synchronises with the device (it copies the word back);
+ * call it after the work it should cover has been synchronised.
+ */
+ZPP_API zpp_status zpp_device_fault(uint32_t* flags, int32_t clear);
+
+/*
+ * Diagnostic (no counterpart in the pages): launches one warp that waits on a
+ * shared-memory barrier nothing completes, bounded by limit_ns nanoseconds (1 ns .. 10 s,
+ * else ZPP_ERR_INVALID_ARG), then sets bit 4 of the fault word and ends. It exercises the
+ * bounded wait and the fault report on the device without a fault of any kind.
+ */
+ZPP_API zpp_status zpp_wait_selftest(uint64_t limit_ns, cudaStream_t stream);
+
+/*
  * Measurement helper (no counterpart in the pages): a 256-bit streaming device copy
  * used as the same-run HBM reference next to the kernels above.
  *   src, dst : 32-byte aligned device buffers; bytes: a multiple of 32.

@@ -64,6 +64,8 @@ def lib():
         "zpp_dequant_reduce_scaled_range": [vp, vp, i64, i32, i32, Topology, LocalRange,
                                             ctypes.c_float, vp, i32, vp],
         "zpp_device_copy": [vp, vp, i64, vp],
+        "zpp_device_fault": [ctypes.POINTER(ctypes.c_uint32), i32],
+        "zpp_wait_selftest": [ctypes.c_uint64, vp],
     }
     for name, args in sig.items():
         f = getattr(L, name)
@@ -145,6 +147,17 @@ def zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, 
 
 def zpp_device_copy(src, dst, nbytes, stream=0):
     return lib().zpp_device_copy(src, dst, nbytes, stream)
+
+
+def zpp_device_fault(clear=False):
+    """The device fault word (see include/zpp.h); synchronises with the device."""
+    v = ctypes.c_uint32(0)
+    _check(lib().zpp_device_fault(ctypes.byref(v), 1 if clear else 0), "zpp_device_fault")
+    return int(v.value)
+
+
+def zpp_wait_selftest(limit_ns, stream=0):
+    return lib().zpp_wait_selftest(limit_ns, stream)
 
 
 def zpp_code_bytes(n, bits):

@@ -26,14 +26,14 @@ namespace zpp {
 // Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
 // in K5; a CTA tile is 8 warps x one row.
 //
-// K4 kernels, chosen per launch by run_drr (all give the same bits):
-//   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  M = KC in {2, 4, 8} or M = 16: the
+// K4 kernels, chosen per launch by drr_bits / run_drr (all give the same bits):
+//   k_dequant_reduce_requant_ring8<KC>          INT8 codes, any M: the bulk-copy ring below;
+//   k_dequant_reduce_requant_staged<4, KC, SPLIT>  INT4, M = KC in {2, 4, 8} or M = 16: the
 //       full CTA tiles, the sources' codes staged in shared memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<BITS, KC, EXACT>   everything else: M = 1, M not a multiple
-//       of its chunk, INT8 M a multiple of 8 above 16, and the ragged last tile of an INT8
-//       or a 2-source staged launch.
+//   k_dequant_reduce_requant<4, KC, EXACT>      INT4 otherwise: M = 1, M not a multiple of
+//       its chunk, and the ragged last tile of a 2-source staged launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
@@ -286,6 +286,211 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
                              r * (C >> log2b), out_codes, out_scales, red);
 }
 
+// ---------------------------------------------------------------------------------
+// K4 for INT8 codes: a bulk-copy ring. One CTA per SM; 16 consumer warps and one producer
+// warp. A unit is 8192 consecutive outputs of one receiver (16 warps x 32 lanes x 16
+// codes); the units are dealt to the CTAs round robin. The producer streams each unit's
+// sources, KC at a time, into a ring of NS shared-memory stages with cp.async.bulk (one
+// 8 KB copy per source: 16 warps x 512 B) plus the matching block scales, each stage
+// completed by an mbarrier; the consumers read their 16 code bytes per source from the
+// stage, accumulate exactly as the other K4 kernels do, release the stage (a second
+// mbarrier) and requantise. INT8 codes carry half the terms per byte of INT4 codes, so
+// this kernel is bound by memory, and the ring keeps the loads in flight while the
+// consumers compute: measured on GB300 at 2^30 INT8 codes, K = 8 / 16, 184 / 166 us
+// against 205 / 213 us for the per-CTA staged kernel. (For INT4 codes the same ring
+// measured 80-88 us on the 4 x 8 bucket against 68 us for the staged kernel: there the
+// conversion work needs the 32 warps per SM that a producer warp would not leave room
+// for.)
+//
+// Every wait is bounded (kRingWaitNs); a wait that runs out sets a bit of g_zpp_fault,
+// and the warp continues without waiting (its results are then unspecified), so the
+// kernel always ends. Before the CTA exits the producer waits (bounded) for the copies it
+// issued that no consumer waited for.
+// ---------------------------------------------------------------------------------
+__device__ unsigned int g_zpp_fault;
+
+constexpr unsigned long long kRingWaitNs = 1000000000ull;  // 1 s
+constexpr int kRingConsumers = 16;
+constexpr int kRingThreads = (kRingConsumers + 1) * 32;
+constexpr int kRingEpl = 16;                           // INT8 codes per lane
+constexpr int kRingRow = 32 * kRingEpl;                // 512 outputs per warp
+constexpr int kRingTile = kRingConsumers * kRingRow;   // 8192 outputs per unit
+constexpr int kRingSrcBytes = kRingTile;               // code bytes per source per unit
+constexpr int kRingScaleSlots = kRingTile / 64;        // scales per source per unit (block >= 64)
+
+template <int KC>
+struct RingGeo {
+  static constexpr int STAGES = KC == 8 ? 3 : (KC == 4 ? 6 : (KC == 2 ? 12 : 24));
+  static constexpr int CODES = STAGES * KC * kRingSrcBytes;
+  static constexpr int SCALES = STAGES * KC * kRingScaleSlots * 4;
+  static constexpr int SMEM = CODES + SCALES + 2 * STAGES * 8 + 2 * 32 * 4;
+};
+
+// Grid: persistent CTAs. Units u = blockIdx.x, blockIdx.x + gridDim.x, ... < U, where
+// U = N * (l_end - l_begin) * T, T = ceil(C / kRingTile); unit u is tile x = u % T of the
+// receiver with index u / T among those with local index in [l_begin, l_end).
+template <int KC>
+__global__ void __launch_bounds__(kRingThreads, 1)
+    k_dequant_reduce_requant_ring8(const uint8_t* __restrict__ codes,
+                                   const float* __restrict__ scales, int64_t E, int log2b, int N,
+                                   int M, int l_begin, int l_end, uint8_t* __restrict__ out_codes,
+                                   float* __restrict__ out_scales) {
+  using G = RingGeo<KC>;
+  constexpr int NS = G::STAGES;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* st_codes = smem;                                         // [NS][KC][kRingSrcBytes]
+  float* st_scales = reinterpret_cast<float*>(smem + G::CODES);     // [NS][KC][kRingScaleSlots]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::CODES + G::SCALES);
+  uint64_t* empty = full + NS;
+  float* red = reinterpret_cast<float*>(empty + NS);  // [2][32] per-warp absmax
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1 + 32);  // the producer's expect_tx arrival + 32 lanes' scale copies
+      mbar_init(&empty[s], kRingConsumers);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  const int64_t C = E / M;
+  const int L = l_end - l_begin;
+  const uint32_t T = static_cast<uint32_t>((C + kRingTile - 1) / kRingTile);
+  const uint32_t U = static_cast<uint32_t>(N) * L * T;
+  const int groups = M / KC;
+
+  if (warp == kRingConsumers) {  // producer
+    const int64_t cb_in = E, sc_in = E >> log2b;  // INT8: one code byte per element
+    int s = 0;
+    unsigned phase = 1;  // a fresh barrier counts its (virtual) previous phase as complete
+    bool ok = true;
+    uint32_t issued = 0;
+    for (uint32_t u = blockIdx.x; u < U && ok; u += gridDim.x) {
+      const uint32_t rho = u / T, x = u - rho * T;
+      const int n = static_cast<int>(rho / L), l = l_begin + static_cast<int>(rho - n * L);
+      const int64_t e0 = static_cast<int64_t>(x) * kRingTile;
+      const int valid = static_cast<int>(C - e0 < kRingTile ? C - e0 : kRingTile);
+      const int64_t idx = static_cast<int64_t>(l) * C + e0;  // chunk l of each source
+      const uint8_t* csrc = codes + static_cast<int64_t>(n) * M * cb_in + idx;
+      const float* ssrc = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
+      const int nsc = valid >> log2b;  // whole blocks: C and e0 are multiples of the block
+      for (int g = 0; g < groups; ++g) {
+        if (!mbar_try_wait(&empty[s], phase) && !mbar_wait_bounded(&empty[s], phase, kRingWaitNs)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], static_cast<unsigned>(valid) * KC);
+#pragma unroll
+          for (int i = 0; i < KC; ++i)
+            bulk_load(st_codes + (s * KC + i) * kRingSrcBytes,
+                      csrc + static_cast<int64_t>(g * KC + i) * cb_in, static_cast<unsigned>(valid),
+                      &full[s]);
+        }
+        for (int j = lane; j < KC * nsc; j += 32) {
+          const int i = j / nsc, b = j - i * nsc;
+          cp_async4(st_scales + (s * KC + i) * kRingScaleSlots + b,
+                    ssrc + static_cast<int64_t>(g * KC + i) * sc_in + b);
+        }
+        cp_async_arrive_noinc(&full[s]);
+        ++issued;
+        if (++s == NS) s = 0, phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) atomicOr(&g_zpp_fault, 1u);
+    // The stages issued last may not have been waited for by any consumer (after a
+    // timeout): wait for them, bounded, before the CTA may exit.
+    unsigned dphase = phase ^ 1u;
+    int ds = s;
+    for (uint32_t d = 0; d < static_cast<uint32_t>(NS) && d < issued; ++d) {
+      if (--ds < 0) ds = NS - 1, dphase ^= 1u;
+      if (!mbar_try_wait(&full[ds], dphase)) mbar_wait_bounded(&full[ds], dphase, kRingWaitNs);
+    }
+    return;
+  }
+
+  const int B = 1 << log2b;
+  const int lane_e = warp * kRingRow + lane * kRingEpl;  // output offset within a unit
+  const int sidx = lane_e >> log2b;
+  const int lane_c = (warp * 32 + lane) * 16;
+  int s = 0;
+  unsigned phase = 0;
+  int ub = 0;
+  bool alive = true;  // false once a wait ran out: no more waits, results unspecified
+  for (uint32_t u = blockIdx.x; u < U; u += gridDim.x, ub ^= 1) {
+    f32x2 acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = f2(0.0f, 0.0f);
+    for (int g = 0; g < groups; ++g) {
+      if (!mbar_try_wait(&full[s], phase) && alive &&
+          !mbar_wait_bounded(&full[s], phase, kRingWaitNs)) {
+        alive = false;
+        if (lane == 0) atomicOr(&g_zpp_fault, 2u);
+      }
+      const uint8_t* cs = st_codes + s * (KC * kRingSrcBytes) + lane_c;
+      const float* ss = st_scales + s * (KC * kRingScaleSlots) + sidx;
+#pragma unroll
+      for (int i = 0; i < KC; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(cs + i * kRingSrcBytes);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        accumulate<8, 4, 0>(acc, w, ss[i * kRingScaleSlots]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == NS) s = 0, phase ^= 1u;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a, b;
+      f2_split(acc[j], a, b);
+      m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+    }
+    if (B <= kRingRow) {
+      m = warp_max(m, B / kRingEpl);
+    } else {  // a block spans B / kRingRow consumer warps of the unit
+      m = warp_max(m, 32);
+      if (lane == 0) red[ub * 32 + warp] = m;
+      named_barrier(1, kRingConsumers * 32);
+      const int wpb = B / kRingRow, w0 = warp & ~(wpb - 1);
+      m = red[ub * 32 + w0];
+      for (int i = 1; i < wpb; ++i) m = fmaxf(m, red[ub * 32 + w0 + i]);
+    }
+    float sc, iv;
+    block_scale<8>(m, sc, iv);
+    const uint32_t rho = u / T, x = u - rho * T;
+    const int n = static_cast<int>(rho / L), l = l_begin + static_cast<int>(rho - n * L);
+    const int64_t e = static_cast<int64_t>(x) * kRingTile + lane_e;
+    if (e < C) {  // C is a multiple of the block: whole blocks are in or out
+      const f32x2 iv2 = f2(iv, iv);
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const f32x2 q[2] = {round_codes(acc[2 * k], iv2), round_codes(acc[2 * k + 1], iv2)};
+        w[k] = pack_int8x4(q);
+      }
+      const int64_t o = (static_cast<int64_t>(n) * M + l) * C + e;  // receiver r = n*M + l
+      st_v4(out_codes + o, make_uint4(w[0], w[1], w[2], w[3]));
+      if ((e & (B - 1)) == 0) out_scales[o >> log2b] = sc;
+    }
+  }
+}
+
+// Diagnostic: a wait on an mbarrier that nothing completes, bounded by limit_ns; sets bit 4
+// of g_zpp_fault when it runs out (it always does). Exercises the bounded wait and the
+// fault word on the device without a fault of any kind.
+__global__ void k_wait_selftest(unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_try_wait(&bar, 0) && !mbar_wait_bounded(&bar, 0, limit_ns))
+    atomicOr(&g_zpp_fault, 4u);
+}
+
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
 // slice: the sums, multiplied by post_scale (1 for the plain sum, 1/W for the average; one
 // fp32 rounding), are written with 256-bit stores as fp32 (each store a full 32-byte
@@ -399,14 +604,42 @@ static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int
   return cudaGetLastError();
 }
 
+template <int KC>
+static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, int log2b, int N,
+                            int M, int lb, int le, void* out_codes, float* out_scales,
+                            cudaStream_t s) {
+  auto kern = k_dequant_reduce_requant_ring8<KC>;
+  constexpr int smem = RingGeo<KC>::SMEM;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return err;
+  const int64_t C = E / M;
+  const int64_t T = (C + kRingTile - 1) / kRingTile;
+  const int64_t U = static_cast<int64_t>(N) * (le - lb) * T;
+  const unsigned grid = static_cast<unsigned>(U < sms ? U : sms);
+  kern<<<grid, kRingThreads, smem, s>>>(static_cast<const uint8_t*>(codes), scales, E, log2b, N,
+                                        M, lb, le, static_cast<uint8_t*>(out_codes), out_scales);
+  return cudaGetLastError();
+}
+
 template <int BITS>
 static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
                             int lb, int le, void* oc, float* os, cudaStream_t s) {
-  switch (chunk_for(M)) {
-    case 8: return run_drr<BITS, 8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    case 4: return run_drr<BITS, 4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    case 2: return run_drr<BITS, 2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    default: return run_drr<BITS, 1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+  if constexpr (BITS == 8) {  // the bulk-copy ring, for any M (sources in groups of KC)
+    if (M % 8 == 0) return run_ring8<8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    if (M % 4 == 0) return run_ring8<4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    if (M % 2 == 0) return run_ring8<2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    return run_ring8<1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+  } else {
+    switch (chunk_for(M)) {
+      case 8: return run_drr<BITS, 8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+      case 4: return run_drr<BITS, 4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+      case 2: return run_drr<BITS, 2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+      default: return run_drr<BITS, 1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    }
   }
 }
 
@@ -437,6 +670,18 @@ cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales
                                  out_scales, s)
                    : drr_bits<4>(codes, scales, E, log2b, N, M, l_begin, l_end, out_codes,
                                  out_scales, s);
+}
+
+cudaError_t read_device_fault(unsigned* flags, bool clear) {
+  cudaError_t err = cudaMemcpyFromSymbol(flags, g_zpp_fault, sizeof(unsigned));
+  if (err != cudaSuccess || !clear) return err;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_zpp_fault, &zero, sizeof(unsigned));
+}
+
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,

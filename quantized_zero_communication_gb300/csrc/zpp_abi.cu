@@ -234,6 +234,19 @@ zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t el
                                          full_range(topo), 1.0f, out, ZPP_F32, stream);
 }
 
+zpp_status zpp_device_fault(uint32_t* flags, int32_t clear) {
+  if (!flags) return ZPP_ERR_INVALID_ARG;
+  unsigned v = 0;
+  const zpp_status st = from_cuda(zpp::read_device_fault(&v, clear != 0));
+  *flags = st == ZPP_OK ? v : 0u;
+  return st;
+}
+
+zpp_status zpp_wait_selftest(uint64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return ZPP_ERR_INVALID_ARG;
+  return from_cuda(zpp::launch_wait_selftest(limit_ns, stream));
+}
+
 zpp_status zpp_device_copy(const void* src, void* dst, int64_t bytes, cudaStream_t stream) {
   if (bytes < 0 || bytes % 32 != 0) return ZPP_ERR_INVALID_ARG;
   if (bytes == 0) return ZPP_OK;

@@ -48,6 +48,14 @@ cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_
                                   int bits, int N, int M, int l_begin, int l_end, float post_scale,
                                   void* out, int out_kind, cudaStream_t s);
 
+// The device fault word: bits set by kernels whose bounded waits ran out (1: a producer
+// wait of the INT8 K4 ring, 2: a consumer wait of that ring, 4: the wait self-test).
+// Synchronous: copies the word of the current device to *flags, then zeroes it if clear.
+cudaError_t read_device_fault(unsigned* flags, bool clear);
+
+// A kernel that waits, bounded by limit_ns, on a barrier nothing completes (sets bit 4).
+cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s);
+
 // K6: 256-bit device copy (the same-run HBM reference).
 cudaError_t launch_copy(const void* src, void* dst, int64_t bytes, cudaStream_t s);
 

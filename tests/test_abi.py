@@ -161,6 +161,13 @@ def test_tensor_bucket_entry_point_rejects_bad_tables():
     assert call([0, 0], [0, 0]) == zb.ZPP_OK                         # empty bucket: no launch
 
 
+def test_fault_query_and_wait_selftest_reject_bad_arguments():
+    L = zb.lib()
+    assert L.zpp_device_fault(None, 0) == zb.ZPP_ERR_INVALID_ARG
+    assert L.zpp_wait_selftest(0, None) == zb.ZPP_ERR_INVALID_ARG
+    assert L.zpp_wait_selftest(10_000_000_001, None) == zb.ZPP_ERR_INVALID_ARG
+
+
 def test_copy_rejects_bad_sizes():
     assert zb.zpp_device_copy(FAKE, FAKE * 2, 33) == zb.ZPP_ERR_INVALID_ARG
     assert zb.zpp_device_copy(FAKE, FAKE * 2, 0) == zb.ZPP_OK

@@ -171,7 +171,10 @@ def run_qgz(g, block, bits, N, M):
     c0, s0 = zpp.qgz_reorder_quant(g, block, bits, N, M)
     c1, s1 = zpp.dequant_reduce_requant(c0, s0, E, block, bits, N, M)
     out = zpp.dequant_reduce(c1, s1, E, block, bits, N, M)
-    return [host(t) for t in (c0, s0, c1, s1, out)]
+    res = [host(t) for t in (c0, s0, c1, s1, out)]
+    # no bounded wait of the INT8 fused hop ran out
+    assert zb.zpp_device_fault() == 0
+    return res
 
 
 def check_qgz(g, block, bits, N, M):
@@ -196,6 +199,20 @@ def test_qgz_pipeline_topologies(N, M, bits):
             g = inputs.draw("laplace", W * E, seed=W + block, dtype=torch.bfloat16,
                             device=DEV).reshape(W, E)
             check_qgz(g, block, bits, N, M)
+
+
+def test_bounded_wait_reports_and_the_context_stays_usable():
+    """A wait that nothing completes ends after its limit and sets its fault bit; the
+    device keeps working afterwards (an INT8 exchange then matches the oracle and leaves
+    the fault word clear)."""
+    zb.zpp_device_fault(clear=True)
+    assert zb.zpp_wait_selftest(20_000_000, torch.cuda.current_stream().cuda_stream) == zb.ZPP_OK
+    torch.cuda.synchronize()
+    assert zb.zpp_device_fault(clear=True) == 4
+    assert zb.zpp_device_fault() == 0
+    g = inputs.draw("laplace", 8 * 8 * 4096, seed=5, dtype=torch.bfloat16,
+                    device=DEV).reshape(8, 8 * 4096)
+    check_qgz(g, 256, 8, 2, 4)
 
 
 # ----------------------------------------------------------------------- fused bucket flatten
