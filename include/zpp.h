@@ -37,8 +37,10 @@
  *   - Inputs and outputs must not overlap.
  *   - Arguments are checked on the host before any launch; on an error nothing is
  *     launched and nothing is written.
- *   - Alignment: element and code buffers (x, y, grads, codes, out) must be 32-byte
- *     aligned (the kernels move 256-bit vectors); scale arrays 4-byte aligned.
+ *   - Alignment: element and code buffers (x, y, grads, codes, out, and the tensors of
+ *     zpp_qgz_reorder_quant_tensors) must be 16-byte aligned; scale arrays 4-byte
+ *     aligned. Element buffers that are also 32-byte aligned take 256-bit vector accesses,
+ *     16-byte aligned ones 128-bit accesses; the results are the same bits.
  *   - n == 0 (or a zero-sized topology payload) returns ZPP_OK and launches nothing.
  *   - A launch failure is reported as ZPP_ERR_CUDA (from cudaGetLastError); an
  *     asynchronous fault surfaces at the caller's next synchronisation.
@@ -146,7 +148,7 @@ ZPP_API zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int6
  * tensors 0..num_tensors-1 ([ZeRO++ summary] Approach: slices reordered for correct
  * placement). The flattening copy -- a full read and write of the bucket -- is saved.
  *   tensors     : HOST array [num_tensors] of device pointers; tensor t holds the W ranks'
- *                 copies back to back ([W][sizes[t]] elements of g_dt), 32-byte aligned
+ *                 copies back to back ([W][sizes[t]] elements of g_dt), 16-byte aligned
  *   sizes       : HOST array [num_tensors], elements per rank of tensor t: a multiple of
  *                 16 (else ZPP_ERR_MISALIGNED), 0 allowed (its pointer is then not read)
  *   num_tensors : 1 .. ZPP_MAX_TENSORS

@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzpp.so")
-SOURCES = ["zpp_abi.cu", "quant.cu", "dequant.cu", "qgz.cu"]
+SOURCES = ["zpp_abi.cu", "quant.cu", "reorder_quant.cu", "reorder_tensors_f16.cu",
+           "reorder_tensors_bf16.cu", "dequant.cu", "qgz.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++20", "-O3", "-lineinfo", "-fmad=false", "-prec-div=true", "-prec-sqrt=true",
          "-ftz=false", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

@@ -65,7 +65,7 @@ __device__ __forceinline__ void store1(void* y, int64_t e, float v) {
     static_cast<__nv_bfloat16*>(y)[e] = __float2bfloat16_rn(v);
 }
 
-template <int BITS, typename OT>
+template <int BITS, typename OT, bool V8>
 __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict__ codes,
                                                       const float* __restrict__ scales,
                                                       int64_t n, int log2b, void* __restrict__ y) {
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
       const int64_t e = t * kDqTile + u * kDqRow + lane * kDqVec;
       float v[kDqVec];
       dequant16<BITS>(w[u], s[u], v);
-      store16<OT>(y, e, v);
+      store16<OT, V8>(y, e, v);
     }
   } else if (t == full) {
     // Ragged end: element-wise.
@@ -101,10 +101,13 @@ __global__ void __launch_bounds__(kThreads) k_dequant(const uint8_t* __restrict_
 template <int BITS, typename OT>
 static cudaError_t run_dequant(const void* codes, const float* scales, int64_t n, int log2b,
                                void* y, cudaStream_t s) {
-  auto kern = k_dequant<BITS, OT>;
   const int64_t tiles = (n + kDqTile - 1) / kDqTile;
   const int grid = tile_grid(tiles, kWarps);
-  kern<<<grid, kThreads, 0, s>>>(static_cast<const uint8_t*>(codes), scales, n, log2b, y);
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  if ((reinterpret_cast<uintptr_t>(y) & 31) == 0)
+    k_dequant<BITS, OT, true><<<grid, kThreads, 0, s>>>(c, scales, n, log2b, y);
+  else
+    k_dequant<BITS, OT, false><<<grid, kThreads, 0, s>>>(c, scales, n, log2b, y);
   return cudaGetLastError();
 }
 

@@ -495,7 +495,7 @@ __global__ void k_wait_selftest(unsigned long long limit_ns) {
 // slice: the sums, multiplied by post_scale (1 for the plain sum, 1/W for the average; one
 // fp32 rounding), are written with 256-bit stores as fp32 (each store a full 32-byte
 // sector) or rounded to fp16 / bf16.
-template <int BITS, int KC, bool EXACT, typename OT>
+template <int BITS, int KC, bool EXACT, typename OT, bool V8>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t E,
                      int log2b, int N, int M, int l_begin, float post_scale, void* __restrict__ out) {
@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kThreads)
   float v[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) f2_split(f2_mul(acc[j], ps), v[2 * j], v[2 * j + 1]);
-  store16<OT>(out, r * S + e, v);
+  store16<OT, V8>(out, r * S + e, v);
 }
 
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
@@ -595,12 +595,24 @@ static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int
   const int64_t S = E / (static_cast<int64_t>(N) * M);
   const dim3 grid(tile_grid(S, kCta5), le - lb, N);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
-  if (N % KC == 0)
-    k_dequant_reduce<BITS, KC, true, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, lb,
-                                                                   post_scale, out);
-  else
-    k_dequant_reduce<BITS, KC, false, OT><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M, lb,
-                                                                    post_scale, out);
+  // out + (r*S + e) elements stays 32-byte aligned when out is: S and e are multiples of 16
+  const bool v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
+  if (N % KC == 0) {
+    if (v8)
+      k_dequant_reduce<BITS, KC, true, OT, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
+                                                                          lb, post_scale, out);
+    else
+      k_dequant_reduce<BITS, KC, true, OT, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N,
+                                                                           M, lb, post_scale, out);
+  } else {
+    if (v8)
+      k_dequant_reduce<BITS, KC, false, OT, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N,
+                                                                           M, lb, post_scale, out);
+    else
+      k_dequant_reduce<BITS, KC, false, OT, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b,
+                                                                            N, M, lb, post_scale,
+                                                                            out);
+  }
   return cudaGetLastError();
 }
 

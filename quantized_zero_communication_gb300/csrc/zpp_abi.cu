@@ -94,7 +94,7 @@ zpp_status zpp_quant_blockwise(const void* x, zpp_dtype x_dt, int64_t n, int32_t
   if (n == 0) return ZPP_OK;
   if (!x || !codes || !scales) return ZPP_ERR_INVALID_ARG;
   if (x_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
-  if (!aligned(x, 32) || !aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_quant(x, x_dt == ZPP_BF16, n, block, bits, codes, scales, stream));
 }
 
@@ -105,7 +105,7 @@ zpp_status zpp_dequant_blockwise(const void* codes, const float* scales, int64_t
   if (y_dt != ZPP_F16 && y_dt != ZPP_BF16 && y_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
   if (n == 0) return ZPP_OK;
   if (!codes || !scales || !y) return ZPP_ERR_INVALID_ARG;
-  if (!aligned(codes, 32) || !aligned(y, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  if (!aligned(codes, 16) || !aligned(y, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant(codes, scales, n, block, bits, y, static_cast<int>(y_dt), stream));
 }
 
@@ -121,7 +121,7 @@ zpp_status zpp_qgz_reorder_quant_range(const void* grads, zpp_dtype g_dt, int64_
   if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!grads || !codes || !scales) return ZPP_ERR_INVALID_ARG;
   if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
-  if (!aligned(grads, 32) || !aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  if (!aligned(grads, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_reorder_quant(grads, g_dt == ZPP_BF16, elems_per_rank, block, bits,
                                              topo.num_nodes, topo.gpus_per_node, range.begin,
                                              range.end, codes, scales, stream));
@@ -157,8 +157,8 @@ zpp_status zpp_qgz_reorder_quant_tensors(const void* const* tensors, const int64
     if (sizes[t] > 0 && !tensors[t]) return ZPP_ERR_INVALID_ARG;
   if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
   for (int32_t t = 0; t < num_tensors; ++t)
-    if (sizes[t] % 16 != 0 || (sizes[t] > 0 && !aligned(tensors[t], 32))) return ZPP_ERR_MISALIGNED;
-  if (!aligned(codes, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+    if (sizes[t] % 16 != 0 || (sizes[t] > 0 && !aligned(tensors[t], 16))) return ZPP_ERR_MISALIGNED;
+  if (!aligned(codes, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   zpp::TensorTable tab;
   tab.count = num_tensors;
   tab.offs[0] = 0;
@@ -182,7 +182,7 @@ zpp_status zpp_dequant_reduce_requant_range(const void* codes, const float* scal
   if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
   if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!codes || !scales || !out_codes || !out_scales) return ZPP_ERR_INVALID_ARG;
-  if (!aligned(codes, 32) || !aligned(out_codes, 32) || !aligned(scales, 4) ||
+  if (!aligned(codes, 16) || !aligned(out_codes, 16) || !aligned(scales, 4) ||
       !aligned(out_scales, 4))
     return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits,
@@ -212,7 +212,7 @@ zpp_status zpp_dequant_reduce_scaled_range(const void* codes, const float* scale
   if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
   if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
-  if (!aligned(codes, 32) || !aligned(out, 32) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  if (!aligned(codes, 16) || !aligned(out, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
                                               topo.num_nodes, topo.gpus_per_node, range.begin,
                                               range.end, post_scale, out,

@@ -166,6 +166,30 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
   asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// 32 bytes as one 256-bit access (V8: the address is 32-byte aligned) or as two 128-bit
+// accesses (the address is 16-byte aligned).
+template <bool V8>
+__device__ __forceinline__ U8x32 ld_vec32(const void* p) {
+  if constexpr (V8) {
+    return ld_stream_v8(p);
+  } else {
+    const uint4 a = ld_stream_v4(p), b = ld_stream_v4(static_cast<const uint8_t*>(p) + 16);
+    U8x32 r;
+    r.w[0] = a.x, r.w[1] = a.y, r.w[2] = a.z, r.w[3] = a.w;
+    r.w[4] = b.x, r.w[5] = b.y, r.w[6] = b.z, r.w[7] = b.w;
+    return r;
+  }
+}
+template <bool V8>
+__device__ __forceinline__ void st_vec32(void* p, const U8x32& v) {
+  if constexpr (V8) {
+    st_v8(p, v);
+  } else {
+    st_v4(p, make_uint4(v.w[0], v.w[1], v.w[2], v.w[3]));
+    st_v4(static_cast<uint8_t*>(p) + 16, make_uint4(v.w[4], v.w[5], v.w[6], v.w[7]));
+  }
+}
+
 // ---------------------------------------------------------------------------------
 // 16-bit float formats. Tag types select fp16 / bf16 at compile time.
 // ---------------------------------------------------------------------------------
@@ -388,9 +412,10 @@ struct OutF16 {};
 struct OutBF16 {};
 struct OutF32 {};
 
-// 16 consecutive fp32 values -> y[e .. e+16) of type OT (fp32: two 256-bit stores;
-// fp16 / bf16: round to nearest even, one 256-bit store).
-template <typename OT>
+// 16 consecutive fp32 values -> y[e .. e+16) of type OT (fp32: 64 bytes; fp16 / bf16:
+// round to nearest even, 32 bytes), as 256-bit stores when y + e is 32-byte aligned (V8),
+// else as 128-bit stores.
+template <typename OT, bool V8>
 __device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
   if constexpr (std::is_same_v<OT, OutF32>) {
     U8x32 a, b;
@@ -400,14 +425,14 @@ __device__ __forceinline__ void store16(void* y, int64_t e, const float v[16]) {
       b.w[i] = __float_as_uint(v[8 + i]);
     }
     float* p = static_cast<float*>(y) + e;
-    st_v8(p, a);
-    st_v8(p + 8, b);
+    st_vec32<V8>(p, a);
+    st_vec32<V8>(p + 8, b);
   } else {
     using TT = std::conditional_t<std::is_same_v<OT, OutF16>, F16, BF16>;
     U8x32 a;
 #pragma unroll
     for (int i = 0; i < 8; ++i) a.w[i] = pack2(v[2 * i], v[2 * i + 1], TT());
-    st_v8(static_cast<uint16_t*>(y) + e, a);
+    st_vec32<V8>(static_cast<uint16_t*>(y) + e, a);
   }
 }
 

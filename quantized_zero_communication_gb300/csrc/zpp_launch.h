@@ -35,6 +35,13 @@ struct TensorTable {
 cudaError_t launch_reorder_quant_tensors(const TensorTable& tab, int is_bf16, int64_t E, int block,
                                          int bits, int N, int M, void* codes, float* scales,
                                          cudaStream_t s);
+// The same per input type (v8: every tensor pointer is 32-byte aligned).
+cudaError_t launch_reorder_quant_tensors_f16(const TensorTable& tab, int64_t E, int block,
+                                             int bits, int N, int M, bool v8, void* codes,
+                                             float* scales, cudaStream_t s);
+cudaError_t launch_reorder_quant_tensors_bf16(const TensorTable& tab, int64_t E, int block,
+                                              int bits, int N, int M, bool v8, void* codes,
+                                              float* scales, cudaStream_t s);
 
 // K4: intra-node fused dequantise -> fp32 sum over M chunks -> requantise.
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,

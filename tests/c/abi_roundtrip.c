@@ -94,7 +94,7 @@ int main(void) {
   /* rejected before any launch; nothing written */
   CHECK(zpp_quant_blockwise(dx, ZPP_F16, N, 100, 4, dcodes, dscales, 0) == ZPP_ERR_INVALID_ARG, "bad block");
   CHECK(zpp_quant_blockwise(dx, ZPP_F16, N, B, 3, dcodes, dscales, 0) == ZPP_ERR_INVALID_ARG, "bad bits");
-  CHECK(zpp_quant_blockwise((char*)dx + 16, ZPP_F16, 64, B, 4, dcodes, dscales, 0) == ZPP_ERR_MISALIGNED, "misaligned");
+  CHECK(zpp_quant_blockwise((char*)dx + 8, ZPP_F16, 64, B, 4, dcodes, dscales, 0) == ZPP_ERR_MISALIGNED, "misaligned");
   CHECK(zpp_code_bytes(7, 4) == 4 && zpp_num_scales(1000, 256) == 4, "size helpers");
   CHECK(strncmp(zpp_status_string(ZPP_ERR_MISALIGNED), "ZPP_ERR_MISALIGNED", 18) == 0, "status string");
   CHECK(cudaDeviceSynchronize() == cudaSuccess, "device sync");

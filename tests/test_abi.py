@@ -78,12 +78,12 @@ def test_quant_rejects_bad_pointers_sizes_and_types():
     assert q(FAKE, zb.ZPP_F16, 64, 256, 8, FAKE, 0) == zb.ZPP_ERR_INVALID_ARG
     assert q(FAKE, 7, 64, 256, 8, FAKE, FAKE) == zb.ZPP_ERR_INVALID_ARG
     assert q(FAKE, zb.ZPP_F32, 64, 256, 8, FAKE, FAKE) == zb.ZPP_ERR_UNSUPPORTED
-    assert q(FAKE + 16, zb.ZPP_F16, 64, 256, 8, FAKE, FAKE) == zb.ZPP_ERR_MISALIGNED
+    assert q(FAKE + 8, zb.ZPP_F16, 64, 256, 8, FAKE, FAKE) == zb.ZPP_ERR_MISALIGNED
     assert q(FAKE, zb.ZPP_BF16, 64, 256, 8, FAKE + 8, FAKE) == zb.ZPP_ERR_MISALIGNED
     assert q(FAKE, zb.ZPP_BF16, 64, 256, 8, FAKE, FAKE + 2) == zb.ZPP_ERR_MISALIGNED
     assert d(FAKE, FAKE, 64, 256, 8, FAKE, 9) == zb.ZPP_ERR_INVALID_ARG
-    assert d(FAKE + 16, FAKE, 64, 256, 8, FAKE, zb.ZPP_F16) == zb.ZPP_ERR_MISALIGNED
-    assert d(FAKE, FAKE, 64, 256, 8, FAKE + 16, zb.ZPP_F32) == zb.ZPP_ERR_MISALIGNED
+    assert d(FAKE + 8, FAKE, 64, 256, 8, FAKE, zb.ZPP_F16) == zb.ZPP_ERR_MISALIGNED
+    assert d(FAKE, FAKE, 64, 256, 8, FAKE + 8, zb.ZPP_F32) == zb.ZPP_ERR_MISALIGNED
     assert d(FAKE, FAKE + 1, 64, 256, 8, FAKE, zb.ZPP_F32) == zb.ZPP_ERR_MISALIGNED
     assert d(FAKE, FAKE, 0, 256, 8, FAKE, zb.ZPP_F16) == zb.ZPP_OK
 
@@ -107,7 +107,7 @@ def test_qgz_entry_points_reject_bad_topologies():
         assert f(-8 * 128, 128, 4, T(2, 4)) == zb.ZPP_ERR_INVALID_ARG
         assert f(0, 128, 4, T(2, 4)) == zb.ZPP_OK                        # empty: no-op
         assert f(8 * 128, 128, 4, T(2, 4), 0) == zb.ZPP_ERR_INVALID_ARG  # null input
-        assert f(8 * 128, 128, 4, T(2, 4), FAKE + 16) == zb.ZPP_ERR_MISALIGNED
+        assert f(8 * 128, 128, 4, T(2, 4), FAKE + 8) == zb.ZPP_ERR_MISALIGNED
     assert zb.zpp_qgz_reorder_quant(FAKE, zb.ZPP_F32, 1024, 128, 4, T(2, 4), FAKE,
                                     FAKE) == zb.ZPP_ERR_UNSUPPORTED
     R = zb.LocalRange
@@ -126,7 +126,7 @@ def test_qgz_entry_points_reject_bad_topologies():
     assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE, 5) == zb.ZPP_ERR_INVALID_ARG
     assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), float("nan"), FAKE, 2) == zb.ZPP_ERR_INVALID_ARG
     assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), float("inf"), FAKE, 2) == zb.ZPP_ERR_INVALID_ARG
-    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE + 16, 1) == zb.ZPP_ERR_MISALIGNED
+    assert sc(FAKE, FAKE, 1024, 128, 4, T(2, 4), 0.125, FAKE + 8, 1) == zb.ZPP_ERR_MISALIGNED
     assert sc(FAKE, FAKE, 1000, 128, 4, T(2, 4), 0.125, FAKE, 1) == zb.ZPP_ERR_INVALID_ARG
     assert sc(FAKE, FAKE, 0, 128, 4, T(2, 4), 0.125, FAKE, 1) == zb.ZPP_OK
 
@@ -155,8 +155,8 @@ def test_tensor_bucket_entry_point_rejects_bad_tables():
     assert call([FAKE, FAKE], [256, 256], codes=0) == INV
     assert call([FAKE, FAKE], [256, 256], dt=zb.ZPP_F32) == UNS
     assert call([FAKE, FAKE], [264, 248]) == MIS                     # not a multiple of 16
-    assert call([FAKE, FAKE + 16], [256, 256]) == MIS                # pointer not 32-byte aligned
-    assert call([FAKE, FAKE], [256, 256], codes=FAKE + 16) == MIS
+    assert call([FAKE, FAKE + 8], [256, 256]) == MIS                 # pointer not 16-byte aligned
+    assert call([FAKE, FAKE], [256, 256], codes=FAKE + 8) == MIS
     assert call([FAKE, FAKE], [256, 256], scales=FAKE + 2) == MIS
     assert call([0, 0], [0, 0]) == zb.ZPP_OK                         # empty bucket: no launch
 

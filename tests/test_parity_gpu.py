@@ -119,16 +119,80 @@ def test_invalid_arguments_write_nothing():
     x = inputs.draw("normal", 4096, seed=1, dtype=torch.float16, device=DEV)
     buf = torch.full((8192,), 0x5A, dtype=torch.uint8, device=DEV)
     sc = torch.full((64,), -1.0, device=DEV)
-    st = zb.zpp_quant_blockwise(x.data_ptr() + 16, zb.ZPP_F16, 1024, 256, 8, buf.data_ptr(),
+    st = zb.zpp_quant_blockwise(x.data_ptr() + 8, zb.ZPP_F16, 1024, 256, 8, buf.data_ptr(),
                                 sc.data_ptr())
     assert st == zb.ZPP_ERR_MISALIGNED
     st = zb.zpp_quant_blockwise(x.data_ptr(), zb.ZPP_F16, 4096, 96, 8, buf.data_ptr(), sc.data_ptr())
     assert st == zb.ZPP_ERR_INVALID_ARG
-    st = zb.zpp_quant_blockwise(x.data_ptr(), zb.ZPP_F16, 4096, 256, 8, buf.data_ptr() + 16,
+    st = zb.zpp_quant_blockwise(x.data_ptr(), zb.ZPP_F16, 4096, 256, 8, buf.data_ptr() + 8,
                                 sc.data_ptr())
     assert st == zb.ZPP_ERR_MISALIGNED
     torch.cuda.synchronize()
     assert torch.all(buf == 0x5A) and torch.all(sc == -1.0)
+
+
+def at16(shape, dtype):
+    """An uninitialised contiguous tensor whose data starts 16 bytes past a 32-byte boundary
+    (16-byte aligned, not 32-byte aligned)."""
+    n = int(np.prod(shape))
+    es = torch.empty(0, dtype=dtype).element_size()
+    buf = torch.empty(n + 32 // es, dtype=dtype, device=DEV)
+    k = ((16 - buf.data_ptr() % 32) % 32) // es
+    v = buf[k:k + n].view(shape)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("bits", [8, 4])
+def test_sixteen_byte_aligned_buffers_are_served(dtype, bits):
+    """Every entry point on buffers that are 16-byte but not 32-byte aligned (fp16 / bf16
+    input at an 8-element offset) takes its 128-bit path and gives the oracle's bits."""
+    n, B = 3 * 4096 + 512, 256
+    x = at16((n,), dtype)
+    x.copy_(inputs.draw("normal", n, seed=3 + bits, dtype=dtype, device=DEV))
+    codes = at16((zb.zpp_code_bytes(n, bits),), torch.uint8)
+    scales = at16((zb.zpp_num_scales(n, B),), torch.float32)
+    zpp.quant_blockwise(x, B, bits, codes, scales)
+    oc, os_ = oracle.quant_blockwise(bits16(x), odt(dtype), B, bits)
+    assert np.array_equal(host(codes), oc)
+    assert np.array_equal(host(scales).view(np.uint32), os_.view(np.uint32))
+    for ydt in (torch.float16, torch.bfloat16, torch.float32):
+        y = zpp.dequant_blockwise(codes, scales, n, B, bits, y=at16((n,), ydt))
+        oy = oracle.dequant_blockwise(oc, os_, n, B, bits, odt(ydt))
+        assert np.array_equal(host(y.view(torch.uint8)), oy.view(np.uint8))
+
+    N, M = 2, 4
+    W, C = N * M, None
+    E = W * (2 * 8192 + 512)
+    C = E // M
+    g = at16((W, E), dtype)
+    g.copy_(inputs.draw("laplace", W * E, seed=9 + bits, dtype=dtype, device=DEV).reshape(W, E))
+    c0 = at16((W, zb.zpp_code_bytes(E, bits)), torch.uint8)
+    s0 = at16((W, E // B), torch.float32)
+    zpp.qgz_reorder_quant(g, B, bits, N, M, codes=c0, scales=s0)
+    c1 = at16((W, zb.zpp_code_bytes(C, bits)), torch.uint8)
+    s1 = at16((W, C // B), torch.float32)
+    zpp.dequant_reduce_requant(c0, s0, E, B, bits, N, M, out_codes=c1, out_scales=s1)
+    out = zpp.dequant_reduce(c1, s1, E, B, bits, N, M, out=at16((W, E // W), torch.float32))
+    avg = zpp.dequant_reduce_scaled(c1, s1, E, B, bits, N, M, post_scale=1.0 / W,
+                                    out=at16((W, E // W), dtype))
+    want = oracle.qgz_pipeline(bits16(g).reshape(W, E), odt(dtype), B, bits, N, M)
+    for a, b, name in zip((c0, s0, c1, s1), want[:4], ("codes", "scales", "hop-1 codes",
+                                                      "hop-1 scales")):
+        assert np.array_equal(host(a).view(np.uint8), b.view(np.uint8)), name
+    assert_f32_parity(host(out), want[4])
+    wavg = oracle.dequant_reduce_scaled(want[2], want[3], E, B, bits, N, M, 1.0 / W, odt(dtype))
+    assert np.array_equal(bits16(avg).reshape(-1), np.asarray(wavg).reshape(-1).view(np.uint16))
+
+    sizes = inputs.random_sizes(E, 5, seed=bits)
+    tensors = []
+    for t in inputs.split_bucket(g, sizes):
+        v = at16(tuple(t.shape), dtype)
+        v.copy_(t)
+        tensors.append(v)
+    tc, ts = zpp.qgz_reorder_quant_tensors(tensors, B, bits, N, M)
+    assert torch.equal(tc, c0) and torch.equal(ts.view(torch.int32), s0.view(torch.int32))
 
 
 def test_shard_launches_equal_one_launch():
