@@ -173,6 +173,10 @@ def zpp_status_string(status):
 
 
 # ----------------------------------------------------------------------------- tensors
+# The wrappers below check every tensor's element count and dtype against what the call
+# reads or writes, then that all tensors are contiguous CUDA tensors on one device, and
+# raise ValueError before calling into libzpp. Sizes that the C ABI itself rejects (bad
+# bits, block or topology) are left to it and raise ZppError with its status.
 def _torch():
     import torch
     return torch
@@ -183,12 +187,27 @@ def _dt(t):
     return {torch.float16: ZPP_F16, torch.bfloat16: ZPP_BF16, torch.float32: ZPP_F32}[t]
 
 
+def _bytes_dtypes():
+    torch = _torch()
+    return (torch.uint8, torch.int8)
+
+
+def _need(t, name, numel=None, dtypes=None):
+    """t must hold exactly `numel` elements of one of `dtypes` (None: not checked)."""
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected one of {tuple(dtypes)}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+
+
 def _cuda(*ts):
     for t in ts:
         if not t.is_cuda:
             raise ValueError("zpp operates on CUDA tensors only (no CPU path)")
         if not t.is_contiguous():
             raise ValueError("zpp needs contiguous tensors")
+    if any(t.device != ts[0].device for t in ts):
+        raise ValueError("all tensors of a call must be on one device")
 
 
 def _stream(t):
@@ -200,15 +219,34 @@ def _check(status, where):
         raise ZppError(status, where)
 
 
+def _sizes_ok(n, block, bits):
+    return n >= 0 and bits in (4, 8) and block in (64, 128, 256, 512, 1024, 2048, 4096)
+
+
+def _qgz_sizes(E, block, bits, N, M):
+    """(W, C, S) when E fits the topology (else None: the C ABI reports it)."""
+    W = N * M
+    if N < 1 or M < 1 or not _sizes_ok(E, block, bits) or E % (W * block):
+        return None
+    return W, E // M, E // W
+
+
 def quant_blockwise(x, block, bits, codes=None, scales=None):
     """x (fp16/bf16, any shape) -> (codes uint8[code_bytes], scales fp32[num_scales])."""
     torch = _torch()
-    _cuda(x)
     n = x.numel()
+    _need(x, "x", dtypes=(torch.float16, torch.bfloat16))
+    ok = _sizes_ok(n, block, bits)
+    if codes is not None:
+        _need(codes, "codes", zpp_code_bytes(n, bits) if ok else None, _bytes_dtypes())
+    if scales is not None:
+        _need(scales, "scales", zpp_num_scales(n, block) if ok else None, (torch.float32,))
+    _cuda(x, *(t for t in (codes, scales) if t is not None))
     if codes is None:
-        codes = torch.empty(zpp_code_bytes(n, bits), dtype=torch.uint8, device=x.device)
+        codes = torch.empty(max(zpp_code_bytes(n, bits), 0), dtype=torch.uint8, device=x.device)
     if scales is None:
-        scales = torch.empty(zpp_num_scales(n, block), dtype=torch.float32, device=x.device)
+        scales = torch.empty(max(zpp_num_scales(n, block), 0), dtype=torch.float32,
+                             device=x.device)
     _check(zpp_quant_blockwise(x.data_ptr(), _dt(x.dtype), n, block, bits, codes.data_ptr(),
                                scales.data_ptr(), _stream(x)), "zpp_quant_blockwise")
     return codes, scales
@@ -217,9 +255,14 @@ def quant_blockwise(x, block, bits, codes=None, scales=None):
 def dequant_blockwise(codes, scales, n, block, bits, dtype=None, y=None):
     """codes, scales -> y[n] of `dtype` (default fp16)."""
     torch = _torch()
-    _cuda(codes, scales)
+    ok = _sizes_ok(n, block, bits)
+    _need(codes, "codes", zpp_code_bytes(n, bits) if ok else None, _bytes_dtypes())
+    _need(scales, "scales", zpp_num_scales(n, block) if ok else None, (torch.float32,))
+    if y is not None:
+        _need(y, "y", n, (torch.float16, torch.bfloat16, torch.float32))
+    _cuda(codes, scales, *(t for t in (y,) if t is not None))
     if y is None:
-        y = torch.empty(n, dtype=dtype or torch.float16, device=codes.device)
+        y = torch.empty(max(n, 0), dtype=dtype or torch.float16, device=codes.device)
     _check(zpp_dequant_blockwise(codes.data_ptr(), scales.data_ptr(), n, block, bits,
                                  y.data_ptr(), _dt(y.dtype), _stream(codes)),
            "zpp_dequant_blockwise")
@@ -229,13 +272,23 @@ def dequant_blockwise(codes, scales, n, block, bits, dtype=None, y=None):
 def qgz_reorder_quant(grads, block, bits, N, M, codes=None, scales=None):
     """grads [W][E] (fp16/bf16) -> (codes uint8 [W][code_bytes(E)], scales fp32 [W][E/block])."""
     torch = _torch()
-    _cuda(grads)
     W = N * M
+    _need(grads, "grads", dtypes=(torch.float16, torch.bfloat16))
+    if W < 1 or grads.numel() % W:
+        raise ValueError(f"grads: {grads.numel()} elements do not split into {W} ranks")
     E = grads.numel() // W
+    sz = _qgz_sizes(E, block, bits, N, M)
+    if codes is not None:
+        _need(codes, "codes", W * zpp_code_bytes(E, bits) if sz else None, _bytes_dtypes())
+    if scales is not None:
+        _need(scales, "scales", W * (E // block) if sz else None, (torch.float32,))
+    _cuda(grads, *(t for t in (codes, scales) if t is not None))
     if codes is None:
-        codes = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=grads.device)
+        codes = torch.empty((W, max(zpp_code_bytes(E, bits), 0)), dtype=torch.uint8,
+                            device=grads.device)
     if scales is None:
-        scales = torch.empty((W, E // block), dtype=torch.float32, device=grads.device)
+        scales = torch.empty((W, E // block if block > 0 else 0), dtype=torch.float32,
+                             device=grads.device)
     _check(zpp_qgz_reorder_quant(grads.data_ptr(), _dt(grads.dtype), E, block, bits,
                                  Topology(N, M), codes.data_ptr(), scales.data_ptr(),
                                  _stream(grads)), "zpp_qgz_reorder_quant")
@@ -249,35 +302,61 @@ def qgz_reorder_quant_tensors(tensors, block, bits, N, M, codes=None, scales=Non
     torch = _torch()
     if not tensors:
         raise ValueError("qgz_reorder_quant_tensors needs at least one tensor")
-    _cuda(*tensors)
     W = N * M
     dt = tensors[0].dtype
-    if any(t.dtype != dt or t.device != tensors[0].device for t in tensors):
-        raise ValueError("all tensors of a bucket share one dtype and device")
-    if any(t.numel() % W for t in tensors):
+    for i, t in enumerate(tensors):
+        _need(t, f"tensors[{i}]", dtypes=(dt,))
+    _need(tensors[0], "tensors[0]", dtypes=(torch.float16, torch.bfloat16))
+    if W < 1 or any(t.numel() % W for t in tensors):
         raise ValueError("every tensor holds W equal per-rank copies")
     sizes = [t.numel() // W for t in tensors]
     E = sum(sizes)
+    sz = _qgz_sizes(E, block, bits, N, M)
+    if codes is not None:
+        _need(codes, "codes", W * zpp_code_bytes(E, bits) if sz else None, _bytes_dtypes())
+    if scales is not None:
+        _need(scales, "scales", W * (E // block) if sz else None, (torch.float32,))
+    _cuda(*tensors, *(t for t in (codes, scales) if t is not None))
     dev = tensors[0].device
     if codes is None:
-        codes = torch.empty((W, zpp_code_bytes(E, bits)), dtype=torch.uint8, device=dev)
+        codes = torch.empty((W, max(zpp_code_bytes(E, bits), 0)), dtype=torch.uint8, device=dev)
     if scales is None:
-        scales = torch.empty((W, E // block), dtype=torch.float32, device=dev)
+        scales = torch.empty((W, E // block if block > 0 else 0), dtype=torch.float32, device=dev)
     _check(zpp_qgz_reorder_quant_tensors([t.data_ptr() for t in tensors], sizes, _dt(dt), block,
                                          bits, Topology(N, M), codes.data_ptr(), scales.data_ptr(),
                                          _stream(tensors[0])), "zpp_qgz_reorder_quant_tensors")
     return codes, scales
 
 
+def _hop_inputs(codes, scales, E, block, bits, N, M, hop):
+    """Checks the codes / scales a hop reads: hop 1 reads the step-1 buffers ([W][E]
+    elements per rank), hop 2 the hop-1 buffers ([W][C], C = E / M)."""
+    torch = _torch()
+    sz = _qgz_sizes(E, block, bits, N, M)
+    n = None if sz is None else (E if hop == 1 else sz[1])
+    W = N * M
+    _need(codes, "codes", W * zpp_code_bytes(n, bits) if sz else None, _bytes_dtypes())
+    _need(scales, "scales", W * (n // block) if sz else None, (torch.float32,))
+    return sz
+
+
 def dequant_reduce_requant(codes, scales, E, block, bits, N, M, out_codes=None, out_scales=None):
     """Intra-node hop -> (codes uint8 [W][code_bytes(E/M)], scales fp32 [W][E/M/block])."""
     torch = _torch()
-    _cuda(codes, scales)
-    W, C = N * M, E // M
+    sz = _hop_inputs(codes, scales, E, block, bits, N, M, hop=1)
+    W, C = N * M, E // M if M > 0 else 0
+    if out_codes is not None:
+        _need(out_codes, "out_codes", W * zpp_code_bytes(C, bits) if sz else None,
+              _bytes_dtypes())
+    if out_scales is not None:
+        _need(out_scales, "out_scales", W * (C // block) if sz else None, (torch.float32,))
+    _cuda(codes, scales, *(t for t in (out_codes, out_scales) if t is not None))
     if out_codes is None:
-        out_codes = torch.empty((W, zpp_code_bytes(C, bits)), dtype=torch.uint8, device=codes.device)
+        out_codes = torch.empty((W, max(zpp_code_bytes(C, bits), 0)), dtype=torch.uint8,
+                                device=codes.device)
     if out_scales is None:
-        out_scales = torch.empty((W, C // block), dtype=torch.float32, device=codes.device)
+        out_scales = torch.empty((W, C // block if block > 0 else 0), dtype=torch.float32,
+                                 device=codes.device)
     _check(zpp_dequant_reduce_requant(codes.data_ptr(), scales.data_ptr(), E, block, bits,
                                       Topology(N, M), out_codes.data_ptr(), out_scales.data_ptr(),
                                       _stream(codes)), "zpp_dequant_reduce_requant")
@@ -287,10 +366,13 @@ def dequant_reduce_requant(codes, scales, E, block, bits, N, M, out_codes=None, 
 def dequant_reduce(codes, scales, E, block, bits, N, M, out=None):
     """Inter-node hop -> fp32 [W][E/W], each rank's summed owner slice."""
     torch = _torch()
-    _cuda(codes, scales)
+    sz = _hop_inputs(codes, scales, E, block, bits, N, M, hop=2)
     W = N * M
+    if out is not None:
+        _need(out, "out", W * (E // W) if sz else None, (torch.float32,))
+    _cuda(codes, scales, *(t for t in (out,) if t is not None))
     if out is None:
-        out = torch.empty((W, E // W), dtype=torch.float32, device=codes.device)
+        out = torch.empty((W, E // W if W > 0 else 0), dtype=torch.float32, device=codes.device)
     _check(zpp_dequant_reduce(codes.data_ptr(), scales.data_ptr(), E, block, bits, Topology(N, M),
                               out.data_ptr(), _stream(codes)), "zpp_dequant_reduce")
     return out
@@ -301,12 +383,17 @@ def dequant_reduce_scaled(codes, scales, E, block, bits, N, M, post_scale=None, 
     """Inter-node hop with the average folded in: [W][E/W] of `dtype` (default fp32) holding
     fp32(sum * post_scale); post_scale defaults to 1/W (the average over ranks)."""
     torch = _torch()
-    _cuda(codes, scales)
+    sz = _hop_inputs(codes, scales, E, block, bits, N, M, hop=2)
     W = N * M
+    if out is not None:
+        _need(out, "out", W * (E // W) if sz else None,
+              (torch.float16, torch.bfloat16, torch.float32))
+    _cuda(codes, scales, *(t for t in (out,) if t is not None))
     if post_scale is None:
         post_scale = 1.0 / W
     if out is None:
-        out = torch.empty((W, E // W), dtype=dtype or torch.float32, device=codes.device)
+        out = torch.empty((W, E // W if W > 0 else 0), dtype=dtype or torch.float32,
+                          device=codes.device)
     _check(zpp_dequant_reduce_scaled(codes.data_ptr(), scales.data_ptr(), E, block, bits,
                                      Topology(N, M), float(post_scale), out.data_ptr(),
                                      _dt(out.dtype), _stream(codes)), "zpp_dequant_reduce_scaled")
@@ -330,6 +417,17 @@ class QgzBuffers:
                    torch.empty((W, C // block), dtype=torch.float32, device=device),
                    torch.empty((W, E // W), dtype=out_dtype or torch.float32, device=device))
 
+    def check(self, W, E, block, bits, M):
+        """Raise ValueError unless every buffer has the size and dtype of an exchange of W
+        ranks of E elements (the layouts of allocate())."""
+        torch = _torch()
+        C = E // M
+        _need(self.c0, "bufs.c0", W * zpp_code_bytes(E, bits), _bytes_dtypes())
+        _need(self.s0, "bufs.s0", W * (E // block), (torch.float32,))
+        _need(self.c1, "bufs.c1", W * zpp_code_bytes(C, bits), _bytes_dtypes())
+        _need(self.s1, "bufs.s1", W * (C // block), (torch.float32,))
+        _need(self.out, "bufs.out", W * (E // W), (torch.float16, torch.bfloat16, torch.float32))
+
 
 def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=None,
                   n_streams=2, chunks=None):
@@ -343,10 +441,19 @@ def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=N
     hop work fills the SMs that reorder work frees (give `high` the higher priority).
     Returns the buffers (owner slices in ``bufs.out``; fp32 by default)."""
     torch = _torch()
-    _cuda(grads)
     W = N * M
+    _need(grads, "grads", dtypes=(torch.float16, torch.bfloat16))
+    if W < 1 or grads.numel() % W:
+        raise ValueError(f"grads: {grads.numel()} elements do not split into {W} ranks")
     E = grads.numel() // W
-    if bufs is None:
+    if _qgz_sizes(E, block, bits, N, M) is None:
+        raise ValueError("elements per rank must be a multiple of W * block (bits 4 or 8, "
+                         "block a power of two in [64, 4096])")
+    if bufs is not None:
+        bufs.check(W, E, block, bits, M)
+        _cuda(grads, bufs.c0, bufs.s0, bufs.c1, bufs.s1, bufs.out)
+    else:
+        _cuda(grads)
         bufs = QgzBuffers.allocate(W, E, block, bits, M, grads.device)
     main = torch.cuda.current_stream(grads.device)
     if streams is None:
@@ -387,7 +494,9 @@ def qgz_pipelined(grads, block, bits, N, M, post_scale=1.0, bufs=None, streams=N
 
 
 def device_copy(src, dst):
-    _cuda(src, dst)
     nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() < nbytes:
+        raise ValueError(f"dst holds {dst.numel() * dst.element_size()} bytes, src {nbytes}")
+    _cuda(src, dst)
     _check(zpp_device_copy(src.data_ptr(), dst.data_ptr(), nbytes, _stream(src)), "zpp_device_copy")
     return dst
