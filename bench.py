@@ -39,11 +39,14 @@ QGZ_N, QGZ_M, QGZ_BLOCK, QGZ_BITS = 4, 8, 512, 4
 QGZ_ELEMS_PER_RANK = 16_777_216
 KERNELS = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant",
            "K5_dequant_reduce")
-KERNEL_SOURCES = {"K1_quant": ["quant.cu", "zpp_device.cuh"],
+KERNEL_SOURCES = {"K1_quant": ["quant.cu", "quant_tile.cuh", "zpp_device.cuh"],
                   "K2_dequant": ["dequant.cu", "zpp_device.cuh"],
-                  "K3_reorder_quant": ["quant.cu", "zpp_device.cuh"],
+                  "K3_reorder_quant": ["reorder_quant.cu", "quant_tile.cuh", "zpp_device.cuh"],
                   "K4_dequant_reduce_requant": ["qgz.cu", "zpp_device.cuh"],
                   "K5_dequant_reduce": ["qgz.cu", "zpp_device.cuh"]}
+# The kernels the spec throughput target names: quantise (K1, and K3 for the
+# gradients), dequantise (K2) and the fused dequant-reduce-requant (K4).
+TARGET_KERNELS = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant")
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -174,7 +177,64 @@ class ClockSampler:
         reasons = sorted({name for r in inside for name, v in zip(self.FLAGS, r[3])
                           if v.lower().startswith("active")})
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "source": "nvidia-smi"}
+
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's libnvidia-ml, read
+    only) about every millisecond in a thread, so a timed region of a few tens of ms still
+    gets tens of samples. start() returns False when NVML is not usable here."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid):
+        self.uuid, self.rows, self.thread, self.stop_flag = uuid, [], None, False
+
+    def start(self):
+        import ctypes
+        import threading
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if L.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+                return False
+            get_reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint()
+            if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:  # 1 = SM clock
+                return False
+        except (OSError, AttributeError):
+            return False
+        self.max_mhz = float(mx.value)
+
+        def run():
+            mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self.stop_flag:
+                if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and \
+                        get_reasons(h, ctypes.byref(rs)) == 0:
+                    self.rows.append((time.time(), float(mhz.value), int(rs.value)))
+                time.sleep(0.001)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+        return True
+
+    def stop(self, t0, t1):
+        self.stop_flag = True
+        self.thread.join(2)
+        if not self.rows:
+            return None
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        if not inside:  # region shorter than the sampling period: the nearest samples
+            mid = (t0 + t1) / 2
+            inside = sorted(self.rows, key=lambda r: abs(r[0] - mid))[:2]
+        sm = sorted(r[1] for r in inside)
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items()
+                          if r[2] & bit})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(inside), "source": "nvml"}
 
 
 # ----------------------------------------------------------------------------- peaks
@@ -285,8 +345,10 @@ def run_ours(args):
     # Timed region: exactly K steps, events on the launching stream around each kernel.
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(active) + 1)]
               for _ in range(args.steps)]
-    sampler = ClockSampler(_smi_id(dev, local))
-    sampler.start()
+    sampler = NvmlClockSampler(_smi_id(dev, local))
+    if not sampler.start():
+        sampler = ClockSampler(_smi_id(dev, local))
+        sampler.start()
     time.sleep(0.15)
     barrier()
     torch.cuda.synchronize()
@@ -330,6 +392,16 @@ def run_ours(args):
     if copy_gbs:
         for k in active:
             kernels[k]["frac_same_run_copy"] = round(kernels[k]["gbs"] / copy_gbs, 4)
+        roof["frac_same_run_copy"] = kernels[dom]["frac_same_run_copy"]
+    # The copy peak is a 1:1 read/write stream; a kernel whose mix is 2:1 or 1:2 can move
+    # more bytes per second than it, so a fraction above 1 is possible and is flagged here.
+    roof["peak_exceeded"] = kernels[dom]["gbs"] > peak
+    targets = [k for k in TARGET_KERNELS if k in active]
+    weakest = min(targets, key=lambda k: kernels[k]["gbs"] / peak) if targets else None
+    roof_min = None if weakest is None else {
+        "kernel": weakest, "achieved": kernels[weakest]["gbs"], "peak": peak, "unit": "GB/s",
+        "frac": kernels[weakest]["frac"],
+        "frac_same_run_copy": kernels[weakest].get("frac_same_run_copy")}
     overlap = None if args.only else _qgz_overlap(zpp, torch, dev, g, E, c0, s0, c1, s1, out,
                                                   per_kernel_bytes)
     as_tensors = None if args.only else _qgz_tensors(zpp, torch, dev, g, E, c0, s0,
@@ -341,10 +413,16 @@ def run_ours(args):
               "data": "synthetic (seeded N(0,0.02/sqrt(96)) fp16 weights; Laplace(0,1e-4) bf16 "
                       "gradients with 0.01% x100 spikes)",
               "config": workload_config(div, n_qwz, E),
-              "roofline": roof, "kernels": kernels,
+              "roofline": roof, "roofline_min": roof_min, "kernels": kernels,
               "copy_kernel_gbs": round(copy_gbs, 1) if copy_gbs else None,
               "qgz_pipelined": overlap, "qgz_tensors": as_tensors,
               "gpu_launches": len(active) * args.steps, "clocks": clocks}
+    # The metric's two named parts: quantise (qwZ K1) and dequant-reduce-requant (K4).
+    for key, k in (("quant", "K1_quant"), ("drr", "K4_dequant_reduce_requant")):
+        if k in kernels:
+            result[f"{key}_gbs"] = kernels[k]["gbs"]
+            result[f"{key}_frac"] = kernels[k]["frac"]
+            result[f"{key}_gelem_per_s"] = kernels[k]["gelem_per_s"]
     if args.only:
         result["only"] = active[0]
     if not args.no_e2e and not args.only:
@@ -485,6 +563,8 @@ def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, 
     def pinned(shape, dtype):
         return torch.empty(shape, dtype=dtype, pin_memory=True)
 
+    # The device-only results of the timed region, to check the end-to-end outputs against.
+    y_ref, out_ref = y.clone(), out.clone()
     hx = [pinned((per,), x.dtype) for _ in range(pieces)]
     hy = [pinned((per,), y.dtype) for _ in range(pieces)]
     for i in range(pieces):
@@ -542,9 +622,15 @@ def run_e2e(args, zpp, torch, dev, x, g, codes, scales, y, c0, s0, c1, s1, out, 
     ms = max_over_ranks(s.elapsed_time(e), device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (*hx, hg))
     d2h = sum(t.numel() * t.element_size() for t in (*hy, hout))
+    # What came back through the host buffers must be what the device-only path computed.
+    same = all(torch.equal(hy[i].to(dev), y_ref[i * per:(i + 1) * per]) for i in range(pieces))
+    same = same and torch.equal(hout.to(dev), out_ref)
+    if not same:
+        raise RuntimeError("end-to-end outputs differ from the device-only path")
     return {"value": round(world * bytes_step * steps / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(ms / steps, 3), "streams": 3, "weight_pieces": pieces}
+            "ms_per_step": round(ms / steps, 3), "streams": 3, "weight_pieces": pieces,
+            "checked": True}
 
 
 # ----------------------------------------------------------------------------- oracle legs

@@ -36,6 +36,15 @@ def test_bench_line_has_the_contract_keys():
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["unit"] == "GB/s"
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert e2e["checked"] is True  # host outputs equal the device-only path's, bit for bit
+    # the weakest of the target kernels, and the metric's two named parts
+    rmin = d["roofline_min"]
+    targets = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant")
+    assert rmin["kernel"] in targets
+    assert rmin["frac"] == min(d["kernels"][k]["frac"] for k in targets)
+    assert d["quant_gbs"] == d["kernels"]["K1_quant"]["gbs"]
+    assert d["drr_gbs"] == d["kernels"]["K4_dequant_reduce_requant"]["gbs"]
+    assert isinstance(roof["peak_exceeded"], bool)
     assert d["gpu_launches"] == 5 * d["steps"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
     assert set(d["kernels"]) == {"K1_quant", "K2_dequant", "K3_reorder_quant",
