@@ -230,6 +230,52 @@ ZPP_API zpp_status zpp_dequant_reduce_scaled_range(const void* codes, const floa
                                                    void* out, zpp_dtype out_dt,
                                                    cudaStream_t stream);
 
+/*
+ * The three qgZ steps as one real rank runs them, on its own buffers, with the two
+ * all-to-all exchanges between them left to the caller's collectives ([ZeRO++ summary]
+ * Approach: 2-hop all-to-all; the virtual-layout calls above run the same kernels with the
+ * exchanges as index maps). For rank r = n*M + l of topology {N, M}, W = N*M, S = E/W,
+ * C = N*S:
+ *
+ * zpp_qgz_reorder_quant_local -- step 1 on this rank's E gradient elements: exactly row r
+ *   of what zpp_qgz_reorder_quant writes (the reorder does not depend on r). Chunk l' (C
+ *   elements at offset l'*C) of the result is what goes to local peer l' in hop 1; only
+ *   the chunks l' in `range` are written ({0, M}: all), so each can be produced just before
+ *   its send.
+ *   grads : [E] elements of g_dt; codes: out, [zpp_code_bytes(E, bits)]; scales: out, [E/block]
+ *   Rules as for zpp_qgz_reorder_quant_range.
+ *
+ * zpp_dequant_reduce_requant_local -- the fused intra-node hop on the chunks this rank
+ *   received: chunk l of each of its node's M ranks, in local-index order, `sources` = M
+ *   chunks of `chunk` = C elements back to back. Writes exactly row r of what
+ *   zpp_dequant_reduce_requant writes.
+ *   codes : [sources][zpp_code_bytes(chunk, bits)]; scales: [sources][chunk/block]
+ *   out_codes : out, [zpp_code_bytes(chunk, bits)]; out_scales: out, [chunk/block]
+ *
+ * zpp_dequant_reduce_local -- the final inter-node hop on the slices this rank received:
+ *   slice n of the hop-1 output of ranks (n', l), n' = 0..N-1 ascending, `sources` = N
+ *   slices of `slice` = S elements back to back. Writes exactly row r of what
+ *   zpp_dequant_reduce_scaled writes (post_scale 1 and fp32 out: zpp_dequant_reduce).
+ *   codes : [sources][zpp_code_bytes(slice, bits)]; scales: [sources][slice/block]
+ *   out   : out, [slice] elements of out_dt; post_scale: finite
+ *
+ * For the last two: block a power of two in [64, 4096], bits 4 or 8, 1 <= sources <= 65535,
+ * chunk (slice) a multiple of block below 2^31 (0: ZPP_OK, nothing launched), else
+ * ZPP_ERR_INVALID_ARG. Alignment and ownership as for every call.
+ */
+ZPP_API zpp_status zpp_qgz_reorder_quant_local(const void* grads, zpp_dtype g_dt,
+                                               int64_t elems_per_rank, int32_t block, int32_t bits,
+                                               zpp_topology topo, zpp_local_range range,
+                                               void* codes, float* scales, cudaStream_t stream);
+ZPP_API zpp_status zpp_dequant_reduce_requant_local(const void* codes, const float* scales,
+                                                    int64_t chunk, int32_t block, int32_t bits,
+                                                    int32_t sources, void* out_codes,
+                                                    float* out_scales, cudaStream_t stream);
+ZPP_API zpp_status zpp_dequant_reduce_local(const void* codes, const float* scales, int64_t slice,
+                                            int32_t block, int32_t bits, int32_t sources,
+                                            float post_scale, void* out, zpp_dtype out_dt,
+                                            cudaStream_t stream);
+
 /* Bytes of packed codes for n elements: n for INT8, ceil(n/2) for INT4; -1 on bad bits. */
 ZPP_API int64_t zpp_code_bytes(int64_t n, int32_t bits);
 

@@ -49,10 +49,13 @@ def lib():
         L.or_qgz_passthrough.argtypes = [vp, i64, i32, i32, i32, vp]
         L.or_dequant_reduce_scaled.argtypes = [vp, vp, i64, i64, i32, i32, i32, ctypes.c_float,
                                                vp, i32]
+        L.or_dequant_reduce_requant_chunks.argtypes = [vp, vp, i64, i64, i32, i32, vp, vp]
+        L.or_dequant_reduce_chunks.argtypes = [vp, vp, i64, i64, i32, i32, ctypes.c_float, vp,
+                                               i32]
         for name in ("or_quant_blockwise", "or_dequant_blockwise", "or_qgz_reorder_quant",
                      "or_dequant_reduce_requant", "or_dequant_reduce", "or_qgz_passthrough",
-                     "or_dequant_reduce_scaled",
-                     "or_rounding_is_nearest"):
+                     "or_dequant_reduce_scaled", "or_dequant_reduce_requant_chunks",
+                     "or_dequant_reduce_chunks", "or_rounding_is_nearest"):
             getattr(L, name).restype = i32
         if not L.or_rounding_is_nearest():
             raise RuntimeError("oracle requires round-to-nearest floating-point mode")
@@ -208,6 +211,38 @@ def dequant_reduce_scaled(codes1, scales1, E: int, block: int, bits: int, N: int
     if lib().or_dequant_reduce_scaled(_p(codes1), _p(scales1), E, block, bits, N, M,
                                       float(post_scale), _p(out), out_dtype):
         raise MemoryError("oracle scaled dequant-reduce failed")
+    return out
+
+
+def _chunks(codes, scales, length, block, bits):
+    if length % block:
+        raise ValueError("chunk length must be a multiple of the block")
+    codes = _contig(codes, np.uint8).reshape(-1, code_bytes(length, bits))
+    scales = _contig(scales, np.float32).reshape(codes.shape[0], length // block)
+    return codes, scales
+
+
+def dequant_reduce_requant_chunks(codes, scales, length: int, block: int, bits: int):
+    """One receiver's hop 1 on the K chunks it was sent (codes [K][code_bytes(length)],
+    scales [K][length/block], summed in row order) -> (codes [code_bytes(length)],
+    scales [length/block])."""
+    codes, scales = _chunks(codes, scales, length, block, bits)
+    oc = np.zeros(code_bytes(length, bits), np.uint8)
+    os_ = np.zeros(length // block, np.float32)
+    if lib().or_dequant_reduce_requant_chunks(_p(codes), _p(scales), length, block, bits,
+                                              codes.shape[0], _p(oc), _p(os_)):
+        raise MemoryError("oracle chunk requantisation failed")
+    return oc, os_
+
+
+def dequant_reduce_chunks(codes, scales, length: int, block: int, bits: int,
+                          post_scale: float = 1.0, out_dtype: int = F32):
+    """One receiver's hop 2 on the K slices it was sent -> [length] of out_dtype holding
+    fp32(sum * post_scale) (float32, or uint16 bits for fp16 / bf16)."""
+    codes, scales = _chunks(codes, scales, length, block, bits)
+    out = np.zeros(length, _value_dtype(out_dtype))
+    lib().or_dequant_reduce_chunks(_p(codes), _p(scales), length, block, bits, codes.shape[0],
+                                   float(post_scale), _p(out), out_dtype)
     return out
 
 

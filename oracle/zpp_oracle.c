@@ -366,6 +366,47 @@ int or_dequant_reduce_scaled(const uint8_t* codes1, const float* scales1, int64_
   return 0;
 }
 
+/* One receiver's hops on the chunks it was sent, as a real rank runs them after each
+ * all-to-all ([ZeRO++ summary] Approach: dequantise the received chunks, reduce in higher
+ * precision; [LIT-102] Key takeaways). The K received chunks of `len` elements lie back to
+ * back, sources in the order they are summed: codes [K][code_bytes(len)], scales
+ * [K][len/block]. Each output element is acc = fma(q, scale, acc) over k = 0..K-1 from
+ * +0.0f. */
+
+/* Hop 1: the sums requantised by blocks -> out_codes [code_bytes(len)], out_scales. */
+int or_dequant_reduce_requant_chunks(const uint8_t* codes, const float* scales, int64_t len,
+                                     int64_t block, int bits, int K, uint8_t* out_codes,
+                                     float* out_scales) {
+  float* acc = (float*)malloc((size_t)(len > 0 ? len : 1) * sizeof(float));
+  if (!acc) return -1;
+  const int64_t cb = or_code_bytes(len, bits), nb = len / block;
+#pragma omp parallel for schedule(static)
+  for (int64_t e = 0; e < len; ++e) {
+    float a = 0.0f;
+    for (int k = 0; k < K; ++k)
+      a = fmaf((float)code_at(codes + k * cb, bits, e), scales[k * nb + e / block], a);
+    acc[e] = a;
+  }
+  int rc = quant_f32(acc, len, block, bits, out_codes, out_scales);
+  free(acc);
+  return rc;
+}
+
+/* Hop 2: the sums times post_scale (one fp32 rounding), stored as out_dtype -> out [len]. */
+int or_dequant_reduce_chunks(const uint8_t* codes, const float* scales, int64_t len,
+                             int64_t block, int bits, int K, float post_scale, void* out,
+                             int out_dtype) {
+  const int64_t cb = or_code_bytes(len, bits), nb = len / block;
+#pragma omp parallel for schedule(static)
+  for (int64_t e = 0; e < len; ++e) {
+    float a = 0.0f;
+    for (int k = 0; k < K; ++k)
+      a = fmaf((float)code_at(codes + k * cb, bits, e), scales[k * nb + e / block], a);
+    store_value(out, out_dtype, e, a * post_scale);
+  }
+  return 0;
+}
+
 /* The same two hops with quantisation switched off (fp32 pass-through), used to check
  * placement. reorder = 0 skips the slice reordering (the wrong layout). x [W][E] ->
  * out [W][S]. */

@@ -6,7 +6,8 @@ dequant-reduce, behind the C ABI declared in ``include/zpp.h``.
 synthetic workloads. The library is loaded on first use.
 """
 from .binding import (  # noqa: F401
-    Topology, ZppError, dequant_blockwise, dequant_reduce, dequant_reduce_requant,
-    dequant_reduce_scaled, device_copy, LocalRange, QgzBuffers, qgz_pipelined,
-    qgz_reorder_quant, qgz_reorder_quant_tensors, quant_blockwise, zpp_code_bytes, zpp_num_scales,
+    Topology, ZppError, dequant_blockwise, dequant_reduce, dequant_reduce_local,
+    dequant_reduce_requant, dequant_reduce_requant_local, dequant_reduce_scaled, device_copy,
+    LocalRange, QgzBuffers, qgz_pipelined, qgz_reorder_quant, qgz_reorder_quant_local,
+    qgz_reorder_quant_tensors, quant_blockwise, zpp_code_bytes, zpp_num_scales,
     zpp_status_string)

@@ -64,6 +64,10 @@ def lib():
         "zpp_dequant_reduce_scaled_range": [vp, vp, i64, i32, i32, Topology, LocalRange,
                                             ctypes.c_float, vp, i32, vp],
         "zpp_device_copy": [vp, vp, i64, vp],
+        "zpp_qgz_reorder_quant_local": [vp, i32, i64, i32, i32, Topology, LocalRange, vp, vp,
+                                        vp],
+        "zpp_dequant_reduce_requant_local": [vp, vp, i64, i32, i32, i32, vp, vp, vp],
+        "zpp_dequant_reduce_local": [vp, vp, i64, i32, i32, i32, ctypes.c_float, vp, i32, vp],
         "zpp_device_fault": [ctypes.POINTER(ctypes.c_uint32), i32],
         "zpp_wait_selftest": [ctypes.c_uint64, vp],
     }
@@ -143,6 +147,24 @@ def zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, 
                                     post_scale, out, out_dt, stream=0):
     return lib().zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits,
                                                  topo, rng, post_scale, out, out_dt, stream)
+
+
+def zpp_qgz_reorder_quant_local(grads, g_dt, elems_per_rank, block, bits, topo, rng, codes,
+                                scales, stream=0):
+    return lib().zpp_qgz_reorder_quant_local(grads, g_dt, elems_per_rank, block, bits, topo, rng,
+                                             codes, scales, stream)
+
+
+def zpp_dequant_reduce_requant_local(codes, scales, chunk, block, bits, sources, out_codes,
+                                     out_scales, stream=0):
+    return lib().zpp_dequant_reduce_requant_local(codes, scales, chunk, block, bits, sources,
+                                                  out_codes, out_scales, stream)
+
+
+def zpp_dequant_reduce_local(codes, scales, slice_len, block, bits, sources, post_scale, out,
+                             out_dt, stream=0):
+    return lib().zpp_dequant_reduce_local(codes, scales, slice_len, block, bits, sources,
+                                          post_scale, out, out_dt, stream)
 
 
 def zpp_device_copy(src, dst, nbytes, stream=0):
@@ -397,6 +419,82 @@ def dequant_reduce_scaled(codes, scales, E, block, bits, N, M, post_scale=None, 
     _check(zpp_dequant_reduce_scaled(codes.data_ptr(), scales.data_ptr(), E, block, bits,
                                      Topology(N, M), float(post_scale), out.data_ptr(),
                                      _dt(out.dtype), _stream(codes)), "zpp_dequant_reduce_scaled")
+    return out
+
+
+# ------------------------------------------------------------------ one real rank's steps
+def qgz_reorder_quant_local(grads, block, bits, N, M, codes=None, scales=None, chunks=None):
+    """This rank's gradient bucket [E] (fp16/bf16) -> its reordered codes [code_bytes(E)]
+    and scales [E/block]: chunk l' (N*S elements) goes to local peer l' in hop 1. With
+    `chunks` = (begin, end) only those chunks are written (into the given buffers)."""
+    torch = _torch()
+    _need(grads, "grads", dtypes=(torch.float16, torch.bfloat16))
+    E = grads.numel()
+    sz = _qgz_sizes(E, block, bits, N, M)
+    if codes is not None:
+        _need(codes, "codes", zpp_code_bytes(E, bits) if sz else None, _bytes_dtypes())
+    if scales is not None:
+        _need(scales, "scales", E // block if sz else None, (torch.float32,))
+    _cuda(grads, *(t for t in (codes, scales) if t is not None))
+    if codes is None:
+        codes = torch.empty(max(zpp_code_bytes(E, bits), 0), dtype=torch.uint8, device=grads.device)
+    if scales is None:
+        scales = torch.empty(E // block if block > 0 else 0, dtype=torch.float32,
+                             device=grads.device)
+    rng = LocalRange(*(chunks if chunks is not None else (0, M)))
+    _check(zpp_qgz_reorder_quant_local(grads.data_ptr(), _dt(grads.dtype), E, block, bits,
+                                       Topology(N, M), rng, codes.data_ptr(), scales.data_ptr(),
+                                       _stream(grads)), "zpp_qgz_reorder_quant_local")
+    return codes, scales
+
+
+def _received(codes, scales, sources, length, block, bits):
+    torch = _torch()
+    ok = sources >= 1 and _sizes_ok(length, block, bits) and length % block == 0
+    _need(codes, "codes", sources * zpp_code_bytes(length, bits) if ok else None, _bytes_dtypes())
+    _need(scales, "scales", sources * (length // block) if ok else None, (torch.float32,))
+    return ok
+
+
+def dequant_reduce_requant_local(codes, scales, chunk, block, bits, sources, out_codes=None,
+                                 out_scales=None):
+    """The fused intra-node hop on the chunks this rank received ([sources][chunk] codes and
+    scales, sources in local-index order) -> its hop-1 codes [code_bytes(chunk)] and scales."""
+    torch = _torch()
+    ok = _received(codes, scales, sources, chunk, block, bits)
+    if out_codes is not None:
+        _need(out_codes, "out_codes", zpp_code_bytes(chunk, bits) if ok else None, _bytes_dtypes())
+    if out_scales is not None:
+        _need(out_scales, "out_scales", chunk // block if ok else None, (torch.float32,))
+    _cuda(codes, scales, *(t for t in (out_codes, out_scales) if t is not None))
+    if out_codes is None:
+        out_codes = torch.empty(max(zpp_code_bytes(chunk, bits), 0), dtype=torch.uint8,
+                                device=codes.device)
+    if out_scales is None:
+        out_scales = torch.empty(chunk // block if block > 0 else 0, dtype=torch.float32,
+                                 device=codes.device)
+    _check(zpp_dequant_reduce_requant_local(codes.data_ptr(), scales.data_ptr(), chunk, block,
+                                            bits, sources, out_codes.data_ptr(),
+                                            out_scales.data_ptr(), _stream(codes)),
+           "zpp_dequant_reduce_requant_local")
+    return out_codes, out_scales
+
+
+def dequant_reduce_local(codes, scales, slice_len, block, bits, sources, post_scale=1.0,
+                         dtype=None, out=None):
+    """The final inter-node hop on the slices this rank received ([sources][slice_len],
+    nodes in ascending order) -> its owner slice [slice_len] of `dtype` (default fp32),
+    fp32(sum * post_scale)."""
+    torch = _torch()
+    ok = _received(codes, scales, sources, slice_len, block, bits)
+    if out is not None:
+        _need(out, "out", slice_len if ok else None, (torch.float16, torch.bfloat16, torch.float32))
+    _cuda(codes, scales, *(t for t in (out,) if t is not None))
+    if out is None:
+        out = torch.empty(max(slice_len, 0), dtype=dtype or torch.float32, device=codes.device)
+    _check(zpp_dequant_reduce_local(codes.data_ptr(), scales.data_ptr(), slice_len, block, bits,
+                                    sources, float(post_scale), out.data_ptr(), _dt(out.dtype),
+                                    _stream(codes)), "zpp_dequant_reduce_local")
     return out
 
 

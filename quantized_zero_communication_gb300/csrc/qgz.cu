@@ -169,8 +169,8 @@ __device__ __forceinline__ void requant_store(const f32x2* acc, int lane, int wa
 // them through shared memory.
 template <int BITS, int KC, bool EXACT, bool FULL, int SPLIT>
 __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
-                                         const float* __restrict__ scales, int64_t E, int log2b,
-                                         int M, int l_begin, int x_begin,
+                                         const float* __restrict__ scales, int64_t E, int64_t C,
+                                         int log2b, int M, int l_begin, int x_begin,
                                          uint8_t* __restrict__ out_codes,
                                          float* __restrict__ out_scales, float* red) {
   using G = Geo4<BITS>;
@@ -178,7 +178,6 @@ __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
   const int B = 1 << log2b;
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
-  const int64_t C = E / M;  // = N * S, the hop-1 chunk
   const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
   const int64_t cb_out = C * BITS / 8, sc_out = C >> log2b;
   const int64_t e = (static_cast<int64_t>(blockIdx.x) + x_begin) * G::CTA + warp * G::ROW +
@@ -199,36 +198,36 @@ __device__ __forceinline__ void drr_tile(const uint8_t* __restrict__ codes,
 
 template <int BITS, int KC, bool EXACT, int SPLIT>
 __device__ __forceinline__ void drr_body(const uint8_t* __restrict__ codes,
-                                         const float* __restrict__ scales, int64_t E, int log2b,
-                                         int M, int l_begin, int x_begin,
+                                         const float* __restrict__ scales, int64_t E, int64_t C,
+                                         int log2b, int M, int l_begin, int x_begin,
                                          uint8_t* __restrict__ out_codes,
                                          float* __restrict__ out_scales) {
   __shared__ float red[kWarps];
-  const int64_t C = E / M;
   if ((static_cast<int64_t>(blockIdx.x) + x_begin + 1) * Geo4<BITS>::CTA <= C)  // CTA-uniform
-    drr_tile<BITS, KC, EXACT, true, SPLIT>(codes, scales, E, log2b, M, l_begin, x_begin,
+    drr_tile<BITS, KC, EXACT, true, SPLIT>(codes, scales, E, C, log2b, M, l_begin, x_begin,
                                            out_codes, out_scales, red);
   else
-    drr_tile<BITS, KC, EXACT, false, SPLIT>(codes, scales, E, log2b, M, l_begin, x_begin,
+    drr_tile<BITS, KC, EXACT, false, SPLIT>(codes, scales, E, C, log2b, M, l_begin, x_begin,
                                             out_codes, out_scales, red);
 }
 
 template <int BITS, int KC, bool EXACT>
 __global__ void __launch_bounds__(kThreads)
     k_dequant_reduce_requant(const uint8_t* __restrict__ codes, const float* __restrict__ scales,
-                             int64_t E, int log2b, int M, int l_begin, int x_begin,
+                             int64_t E, int64_t C, int log2b, int M, int l_begin, int x_begin,
                              uint8_t* __restrict__ out_codes, float* __restrict__ out_scales) {
-  drr_body<BITS, KC, EXACT, 0>(codes, scales, E, log2b, M, l_begin, x_begin, out_codes,
+  drr_body<BITS, KC, EXACT, 0>(codes, scales, E, C, log2b, M, l_begin, x_begin, out_codes,
                                out_scales);
 }
 
 template <int KC>
 __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
     k_dequant_reduce_requant_split(const uint8_t* __restrict__ codes,
-                                   const float* __restrict__ scales, int64_t E, int log2b, int M,
-                                   int l_begin, int x_begin, uint8_t* __restrict__ out_codes,
+                                   const float* __restrict__ scales, int64_t E, int64_t C,
+                                   int log2b, int M, int l_begin, int x_begin,
+                                   uint8_t* __restrict__ out_codes,
                                    float* __restrict__ out_scales) {
-  drr_body<4, KC, true, kSplitWords>(codes, scales, E, log2b, M, l_begin, x_begin, out_codes,
+  drr_body<4, KC, true, kSplitWords>(codes, scales, E, C, log2b, M, l_begin, x_begin, out_codes,
                                      out_scales);
 }
 
@@ -245,8 +244,8 @@ constexpr int staged_smem_bytes() { return KC * kThreads * 16; }
 template <int BITS, int KC, int SPLIT>
 __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
     k_dequant_reduce_requant_staged(const uint8_t* __restrict__ codes,
-                                    const float* __restrict__ scales, int64_t E, int log2b,
-                                    int l_begin, uint8_t* __restrict__ out_codes,
+                                    const float* __restrict__ scales, int64_t E, int64_t C,
+                                    int log2b, int l_begin, uint8_t* __restrict__ out_codes,
                                     float* __restrict__ out_scales) {
   using G = Geo4<BITS>;
   constexpr int M = KC, H = KC / 2;
@@ -256,7 +255,6 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
-  const int64_t C = E / M;
   const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
   const int64_t e = static_cast<int64_t>(blockIdx.x) * G::CTA + warp * G::ROW + lane * G::EPL;
   const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
@@ -332,8 +330,9 @@ struct RingGeo {
 template <int KC>
 __global__ void __launch_bounds__(kRingThreads, 1)
     k_dequant_reduce_requant_ring8(const uint8_t* __restrict__ codes,
-                                   const float* __restrict__ scales, int64_t E, int log2b, int N,
-                                   int M, int l_begin, int l_end, uint8_t* __restrict__ out_codes,
+                                   const float* __restrict__ scales, int64_t E, int64_t C,
+                                   int log2b, int N, int M, int l_begin, int l_end,
+                                   uint8_t* __restrict__ out_codes,
                                    float* __restrict__ out_scales) {
   using G = RingGeo<KC>;
   constexpr int NS = G::STAGES;
@@ -354,7 +353,6 @@ __global__ void __launch_bounds__(kRingThreads, 1)
   }
   __syncthreads();
 
-  const int64_t C = E / M;
   const int L = l_end - l_begin;
   const uint32_t T = static_cast<uint32_t>((C + kRingTile - 1) / kRingTile);
   const uint32_t U = static_cast<uint32_t>(N) * L * T;
@@ -494,17 +492,18 @@ __global__ void k_wait_selftest(unsigned long long limit_ns) {
 // K5. Grid (tile, l, n) as for K4. A lane owns 16 consecutive outputs of its receiver's
 // slice: the sums, multiplied by post_scale (1 for the plain sum, 1/W for the average; one
 // fp32 rounding), are written with 256-bit stores as fp32 (each store a full 32-byte
-// sector) or rounded to fp16 / bf16.
+// sector) or rounded to fp16 / bf16. S is the slice each receiver owns and C the length of
+// one hop-1 output; the N sources of receiver (n, l) are the hop-1 outputs of ranks
+// (n', l), at a stride of M outputs, from which it reads slice n.
 template <int BITS, int KC, bool EXACT, typename OT, bool V8>
 __global__ void __launch_bounds__(kThreads)
-    k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t E,
-                     int log2b, int N, int M, int l_begin, float post_scale, void* __restrict__ out) {
+    k_dequant_reduce(const uint8_t* __restrict__ codes, const float* __restrict__ scales, int64_t S,
+                     int64_t C, int log2b, int N, int M, int l_begin, float post_scale,
+                     void* __restrict__ out) {
   constexpr int NW = BITS == 8 ? 4 : 2;  // code words per lane per source
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
-  const int64_t W = static_cast<int64_t>(N) * M;
-  const int64_t S = E / W, C = E / M;
   const int64_t cb = C * BITS / 8, sc = C >> log2b;  // per hop-1 rank
   const int64_t e = static_cast<int64_t>(blockIdx.x) * kCta5 + warp * kRow5 + lane * kEpl5;
   if (e >= S) return;  // no barrier in this kernel
@@ -527,9 +526,9 @@ __global__ void __launch_bounds__(kThreads)
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
 
 template <int BITS, int KC, int SPLIT>
-static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, int log2b, int lb,
-                              int64_t full, unsigned ny, unsigned nz, uint8_t* oc,
-                              float* out_scales, cudaStream_t s) {
+static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, int64_t C,
+                              int log2b, int lb, int64_t full, unsigned ny, unsigned nz,
+                              uint8_t* oc, float* out_scales, cudaStream_t s) {
   constexpr int smem = staged_smem_bytes<KC>();
   auto kern = k_dequant_reduce_requant_staged<BITS, KC, SPLIT>;
   if constexpr (smem > 48 * 1024) {  // above the default dynamic shared-memory limit
@@ -537,17 +536,16 @@ static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, 
                                                smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<dim3(static_cast<unsigned>(full), ny, nz), kThreads, smem, s>>>(c, scales, E, log2b, lb,
-                                                                        oc, out_scales);
+  kern<<<dim3(static_cast<unsigned>(full), ny, nz), kThreads, smem, s>>>(c, scales, E, C, log2b,
+                                                                        lb, oc, out_scales);
   return cudaGetLastError();
 }
 
 template <int BITS, int KC>
-static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                           int M, int lb, int le, void* out_codes, float* out_scales,
+static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int64_t C, int log2b,
+                           int N, int M, int lb, int le, void* out_codes, float* out_scales,
                            cudaStream_t s) {
   constexpr int CTA = Geo4<BITS>::CTA;
-  const int64_t C = E / M;
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
   const unsigned ny = static_cast<unsigned>(le - lb), nz = static_cast<unsigned>(N);
@@ -558,68 +556,71 @@ static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, in
       cudaError_t err = cudaSuccess;
       if (full > 0) {
         if (M == KC)
-          err = run_staged<BITS, KC, SPLIT>(c, scales, E, log2b, lb, full, ny, nz, oc, out_scales,
-                                            s);
+          err = run_staged<BITS, KC, SPLIT>(c, scales, E, C, log2b, lb, full, ny, nz, oc,
+                                            out_scales, s);
         else if constexpr (KC == 8)  // M == 16
-          err = run_staged<BITS, 16, SPLIT>(c, scales, E, log2b, lb, full, ny, nz, oc, out_scales,
-                                            s);
+          err = run_staged<BITS, 16, SPLIT>(c, scales, E, C, log2b, lb, full, ny, nz, oc,
+                                            out_scales, s);
       }
       if (err != cudaSuccess) return err;
       if (C % CTA != 0) {
         if constexpr (BITS == 4 && KC >= 4)
           k_dequant_reduce_requant_split<KC><<<dim3(1, ny, nz), kThreads, 0, s>>>(
-              c, scales, E, log2b, M, lb, static_cast<int>(full), oc, out_scales);
+              c, scales, E, C, log2b, M, lb, static_cast<int>(full), oc, out_scales);
         else
           k_dequant_reduce_requant<BITS, KC, true><<<dim3(1, ny, nz), kThreads, 0, s>>>(
-              c, scales, E, log2b, M, lb, static_cast<int>(full), oc, out_scales);
+              c, scales, E, C, log2b, M, lb, static_cast<int>(full), oc, out_scales);
       }
       return cudaGetLastError();
     }
   }
   const dim3 grid(tile_grid(C, CTA), ny, nz);
   if (M % KC != 0)
-    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb,
-                                                                        0, oc, out_scales);
+    k_dequant_reduce_requant<BITS, KC, false><<<grid, kThreads, 0, s>>>(c, scales, E, C, log2b, M,
+                                                                        lb, 0, oc, out_scales);
   else if constexpr (BITS == 4 && KC >= 4)
-    k_dequant_reduce_requant_split<KC><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb, 0, oc,
-                                                                 out_scales);
+    k_dequant_reduce_requant_split<KC><<<grid, kThreads, 0, s>>>(c, scales, E, C, log2b, M, lb, 0,
+                                                                 oc, out_scales);
   else
-    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, M, lb,
-                                                                       0, oc, out_scales);
+    k_dequant_reduce_requant<BITS, KC, true><<<grid, kThreads, 0, s>>>(c, scales, E, C, log2b, M,
+                                                                       lb, 0, oc, out_scales);
   return cudaGetLastError();
 }
 
 template <int BITS, int KC, typename OT>
-static cudaError_t run_dr(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                          int M, int lb, int le, float post_scale, void* out, cudaStream_t s) {
-  const int64_t S = E / (static_cast<int64_t>(N) * M);
-  const dim3 grid(tile_grid(S, kCta5), le - lb, N);
+static cudaError_t run_dr(const void* codes, const float* scales, int64_t S, int64_t C, int log2b,
+                          int N, int M, int lb, int le, int nz, float post_scale, void* out,
+                          cudaStream_t s) {
+  const dim3 grid(tile_grid(S, kCta5), le - lb, nz);
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   // out + (r*S + e) elements stays 32-byte aligned when out is: S and e are multiples of 16
   const bool v8 = (reinterpret_cast<uintptr_t>(out) & 31) == 0;
   if (N % KC == 0) {
     if (v8)
-      k_dequant_reduce<BITS, KC, true, OT, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N, M,
-                                                                          lb, post_scale, out);
+      k_dequant_reduce<BITS, KC, true, OT, true><<<grid, kThreads, 0, s>>>(c, scales, S, C, log2b,
+                                                                          N, M, lb, post_scale,
+                                                                          out);
     else
-      k_dequant_reduce<BITS, KC, true, OT, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N,
-                                                                           M, lb, post_scale, out);
+      k_dequant_reduce<BITS, KC, true, OT, false><<<grid, kThreads, 0, s>>>(c, scales, S, C, log2b,
+                                                                           N, M, lb, post_scale,
+                                                                           out);
   } else {
     if (v8)
-      k_dequant_reduce<BITS, KC, false, OT, true><<<grid, kThreads, 0, s>>>(c, scales, E, log2b, N,
-                                                                           M, lb, post_scale, out);
+      k_dequant_reduce<BITS, KC, false, OT, true><<<grid, kThreads, 0, s>>>(c, scales, S, C, log2b,
+                                                                           N, M, lb, post_scale,
+                                                                           out);
     else
-      k_dequant_reduce<BITS, KC, false, OT, false><<<grid, kThreads, 0, s>>>(c, scales, E, log2b,
-                                                                            N, M, lb, post_scale,
-                                                                            out);
+      k_dequant_reduce<BITS, KC, false, OT, false><<<grid, kThreads, 0, s>>>(c, scales, S, C,
+                                                                            log2b, N, M, lb,
+                                                                            post_scale, out);
   }
   return cudaGetLastError();
 }
 
 template <int KC>
-static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, int log2b, int N,
-                            int M, int lb, int le, void* out_codes, float* out_scales,
-                            cudaStream_t s) {
+static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, int64_t C,
+                            int log2b, int N, int M, int lb, int le, void* out_codes,
+                            float* out_scales, cudaStream_t s) {
   auto kern = k_dequant_reduce_requant_ring8<KC>;
   constexpr int smem = RingGeo<KC>::SMEM;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -628,59 +629,60 @@ static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, 
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return err;
-  const int64_t C = E / M;
   const int64_t T = (C + kRingTile - 1) / kRingTile;
   const int64_t U = static_cast<int64_t>(N) * (le - lb) * T;
   const unsigned grid = static_cast<unsigned>(U < sms ? U : sms);
-  kern<<<grid, kRingThreads, smem, s>>>(static_cast<const uint8_t*>(codes), scales, E, log2b, N,
-                                        M, lb, le, static_cast<uint8_t*>(out_codes), out_scales);
+  kern<<<grid, kRingThreads, smem, s>>>(static_cast<const uint8_t*>(codes), scales, E, C, log2b,
+                                        N, M, lb, le, static_cast<uint8_t*>(out_codes),
+                                        out_scales);
   return cudaGetLastError();
 }
 
 template <int BITS>
-static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
-                            int lb, int le, void* oc, float* os, cudaStream_t s) {
+static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int64_t C, int log2b, int N,
+                            int M, int lb, int le, void* oc, float* os, cudaStream_t s) {
   if constexpr (BITS == 8) {  // the bulk-copy ring, for any M (sources in groups of KC)
-    if (M % 8 == 0) return run_ring8<8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    if (M % 4 == 0) return run_ring8<4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    if (M % 2 == 0) return run_ring8<2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-    return run_ring8<1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+    if (M % 8 == 0) return run_ring8<8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    if (M % 4 == 0) return run_ring8<4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    if (M % 2 == 0) return run_ring8<2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    return run_ring8<1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
   } else {
     switch (chunk_for(M)) {
-      case 8: return run_drr<BITS, 8>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-      case 4: return run_drr<BITS, 4>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-      case 2: return run_drr<BITS, 2>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
-      default: return run_drr<BITS, 1>(c, sc, E, log2b, N, M, lb, le, oc, os, s);
+      case 8: return run_drr<BITS, 8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      case 4: return run_drr<BITS, 4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      case 2: return run_drr<BITS, 2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      default: return run_drr<BITS, 1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
     }
   }
 }
 
 template <int BITS, typename OT>
-static cudaError_t dr_bits(const void* c, const float* sc, int64_t E, int log2b, int N, int M,
-                           int lb, int le, float ps, void* out, cudaStream_t s) {
+static cudaError_t dr_bits(const void* c, const float* sc, int64_t S, int64_t C, int log2b, int N,
+                           int M, int lb, int le, int nz, float ps, void* out, cudaStream_t s) {
   switch (chunk_for(N)) {
-    case 8: return run_dr<BITS, 8, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
-    case 4: return run_dr<BITS, 4, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
-    case 2: return run_dr<BITS, 2, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
-    default: return run_dr<BITS, 1, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
+    case 8: return run_dr<BITS, 8, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s);
+    case 4: return run_dr<BITS, 4, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s);
+    case 2: return run_dr<BITS, 2, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s);
+    default: return run_dr<BITS, 1, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s);
   }
 }
 
 template <typename OT>
-static cudaError_t dr_out(const void* c, const float* sc, int64_t E, int log2b, int bits, int N,
-                          int M, int lb, int le, float ps, void* out, cudaStream_t s) {
-  return bits == 8 ? dr_bits<8, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s)
-                   : dr_bits<4, OT>(c, sc, E, log2b, N, M, lb, le, ps, out, s);
+static cudaError_t dr_out(const void* c, const float* sc, int64_t S, int64_t C, int log2b, int bits,
+                          int N, int M, int lb, int le, int nz, float ps, void* out,
+                          cudaStream_t s) {
+  return bits == 8 ? dr_bits<8, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s)
+                   : dr_bits<4, OT>(c, sc, S, C, log2b, N, M, lb, le, nz, ps, out, s);
 }
 
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
-                                          int block, int bits, int N, int M, int l_begin,
-                                          int l_end, void* out_codes, float* out_scales,
-                                          cudaStream_t s) {
+                                          int64_t C, int block, int bits, int N, int M,
+                                          int l_begin, int l_end, void* out_codes,
+                                          float* out_scales, cudaStream_t s) {
   const int log2b = __builtin_ctz(static_cast<unsigned>(block));
-  return bits == 8 ? drr_bits<8>(codes, scales, E, log2b, N, M, l_begin, l_end, out_codes,
+  return bits == 8 ? drr_bits<8>(codes, scales, E, C, log2b, N, M, l_begin, l_end, out_codes,
                                  out_scales, s)
-                   : drr_bits<4>(codes, scales, E, log2b, N, M, l_begin, l_end, out_codes,
+                   : drr_bits<4>(codes, scales, E, C, log2b, N, M, l_begin, l_end, out_codes,
                                  out_scales, s);
 }
 
@@ -696,15 +698,19 @@ cudaError_t launch_wait_selftest(unsigned long long limit_ns, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, int l_begin, int l_end, float post_scale,
-                                  void* out, int out_kind, cudaStream_t s) {
+cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t S, int64_t C,
+                                  int block, int bits, int N, int M, int l_begin, int l_end,
+                                  int nz, float post_scale, void* out, int out_kind,
+                                  cudaStream_t s) {
   const int log2b = __builtin_ctz(static_cast<unsigned>(block));
   if (out_kind == 0)
-    return dr_out<OutF16>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
+    return dr_out<OutF16>(codes, scales, S, C, log2b, bits, N, M, l_begin, l_end, nz, post_scale,
+                          out, s);
   if (out_kind == 1)
-    return dr_out<OutBF16>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
-  return dr_out<OutF32>(codes, scales, E, log2b, bits, N, M, l_begin, l_end, post_scale, out, s);
+    return dr_out<OutBF16>(codes, scales, S, C, log2b, bits, N, M, l_begin, l_end, nz, post_scale,
+                           out, s);
+  return dr_out<OutF32>(codes, scales, S, C, log2b, bits, N, M, l_begin, l_end, nz, post_scale,
+                        out, s);
 }
 
 }  // namespace zpp

@@ -40,13 +40,13 @@ __global__ void __launch_bounds__(kThreads) k_reorder_quant(const uint16_t* __re
 
 template <typename TT, int BITS, int B, bool V8>
 static cudaError_t run_reorder_quant(const void* g, int64_t E, int N, int M, int l_begin, int l_end,
-                                     void* codes, float* scales, cudaStream_t s) {
+                                     int ranks, void* codes, float* scales, cudaStream_t s) {
   auto kern = k_reorder_quant<TT, BITS, B, V8>;
   const int64_t W = static_cast<int64_t>(N) * M, S = E / W;
   const int64_t tps = (S + QuantTile<B>::TILE - 1) / QuantTile<B>::TILE;
   // output slice positions of chunks l_begin .. l_end-1: p in [l_begin*N, l_end*N)
   const dim3 grid(tile_grid(tps, kWarps), static_cast<unsigned>((l_end - l_begin) * N),
-                  static_cast<unsigned>(W));
+                  static_cast<unsigned>(ranks));
   kern<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t*>(g), E, N, M, l_begin * N,
                                  static_cast<uint8_t*>(codes), scales);
   return cudaGetLastError();
@@ -62,11 +62,12 @@ cudaError_t launch_reorder_quant_tensors(const TensorTable& tab, int is_bf16, in
 }
 
 cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block, int bits,
-                                 int N, int M, int l_begin, int l_end, void* codes, float* scales,
-                                 cudaStream_t s) {
+                                 int N, int M, int l_begin, int l_end, int ranks, void* codes,
+                                 float* scales, cudaStream_t s) {
   const bool v8 = (reinterpret_cast<uintptr_t>(grads) & 31) == 0;
   return by_type_bits_block(is_bf16, bits, block, v8, [&]<typename TT, int BITS, int B, bool V8>() {
-    return run_reorder_quant<TT, BITS, B, V8>(grads, E, N, M, l_begin, l_end, codes, scales, s);
+    return run_reorder_quant<TT, BITS, B, V8>(grads, E, N, M, l_begin, l_end, ranks, codes,
+                                              scales, s);
   });
 }
 

@@ -124,7 +124,8 @@ zpp_status zpp_qgz_reorder_quant_range(const void* grads, zpp_dtype g_dt, int64_
   if (!aligned(grads, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
   return from_cuda(zpp::launch_reorder_quant(grads, g_dt == ZPP_BF16, elems_per_rank, block, bits,
                                              topo.num_nodes, topo.gpus_per_node, range.begin,
-                                             range.end, codes, scales, stream));
+                                             range.end, static_cast<int>(W), codes, scales,
+                                             stream));
 }
 
 zpp_status zpp_qgz_reorder_quant(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
@@ -185,10 +186,9 @@ zpp_status zpp_dequant_reduce_requant_range(const void* codes, const float* scal
   if (!aligned(codes, 16) || !aligned(out_codes, 16) || !aligned(scales, 4) ||
       !aligned(out_scales, 4))
     return ZPP_ERR_MISALIGNED;
-  return from_cuda(zpp::launch_dequant_reduce_requant(codes, scales, elems_per_rank, block, bits,
-                                                      topo.num_nodes, topo.gpus_per_node,
-                                                      range.begin, range.end, out_codes,
-                                                      out_scales, stream));
+  return from_cuda(zpp::launch_dequant_reduce_requant(
+      codes, scales, elems_per_rank, elems_per_rank / topo.gpus_per_node, block, bits,
+      topo.num_nodes, topo.gpus_per_node, range.begin, range.end, out_codes, out_scales, stream));
 }
 
 zpp_status zpp_dequant_reduce_requant(const void* codes, const float* scales,
@@ -213,10 +213,10 @@ zpp_status zpp_dequant_reduce_scaled_range(const void* codes, const float* scale
   if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
   if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
   if (!aligned(codes, 16) || !aligned(out, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
-  return from_cuda(zpp::launch_dequant_reduce(codes, scales, elems_per_rank, block, bits,
-                                              topo.num_nodes, topo.gpus_per_node, range.begin,
-                                              range.end, post_scale, out,
-                                              static_cast<int>(out_dt), stream));
+  return from_cuda(zpp::launch_dequant_reduce(
+      codes, scales, elems_per_rank / W, elems_per_rank / topo.gpus_per_node, block, bits,
+      topo.num_nodes, topo.gpus_per_node, range.begin, range.end, topo.num_nodes, post_scale, out,
+      static_cast<int>(out_dt), stream));
 }
 
 zpp_status zpp_dequant_reduce_scaled(const void* codes, const float* scales,
@@ -232,6 +232,70 @@ zpp_status zpp_dequant_reduce(const void* codes, const float* scales, int64_t el
                               cudaStream_t stream) {
   return zpp_dequant_reduce_scaled_range(codes, scales, elems_per_rank, block, bits, topo,
                                          full_range(topo), 1.0f, out, ZPP_F32, stream);
+}
+
+zpp_status zpp_qgz_reorder_quant_local(const void* grads, zpp_dtype g_dt, int64_t elems_per_rank,
+                                       int32_t block, int32_t bits, zpp_topology topo,
+                                       zpp_local_range range, void* codes, float* scales,
+                                       cudaStream_t stream) {
+  int64_t W = 0;
+  zpp_status st = check_topology(elems_per_rank, block, bits, topo, &W);
+  if (st != ZPP_OK) return st;
+  if (g_dt != ZPP_F16 && g_dt != ZPP_BF16 && g_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (!valid_range(range, topo)) return ZPP_ERR_INVALID_ARG;
+  if (elems_per_rank == 0 || range.begin == range.end) return ZPP_OK;
+  if (!grads || !codes || !scales) return ZPP_ERR_INVALID_ARG;
+  if (g_dt == ZPP_F32) return ZPP_ERR_UNSUPPORTED;
+  if (!aligned(grads, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  return from_cuda(zpp::launch_reorder_quant(grads, g_dt == ZPP_BF16, elems_per_rank, block, bits,
+                                             topo.num_nodes, topo.gpus_per_node, range.begin,
+                                             range.end, 1, codes, scales, stream));
+}
+
+namespace {
+// Checks shared by the two calls on received chunks: `len` elements per source, a
+// multiple of the block, `sources` of them.
+zpp_status check_received(int64_t len, int32_t block, int32_t bits, int32_t sources) {
+  if (!valid_bits(bits) || !valid_block(block)) return ZPP_ERR_INVALID_ARG;
+  if (sources < 1 || sources > 65535) return ZPP_ERR_INVALID_ARG;
+  if (len < 0 || len >= (int64_t{1} << 31) || len % block != 0) return ZPP_ERR_INVALID_ARG;
+  if (len * sources > ZPP_MAX_ELEMS) return ZPP_ERR_INVALID_ARG;
+  return ZPP_OK;
+}
+}  // namespace
+
+zpp_status zpp_dequant_reduce_requant_local(const void* codes, const float* scales, int64_t chunk,
+                                            int32_t block, int32_t bits, int32_t sources,
+                                            void* out_codes, float* out_scales,
+                                            cudaStream_t stream) {
+  const zpp_status st = check_received(chunk, block, bits, sources);
+  if (st != ZPP_OK) return st;
+  if (chunk == 0) return ZPP_OK;
+  if (!codes || !scales || !out_codes || !out_scales) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(out_codes, 16) || !aligned(scales, 4) ||
+      !aligned(out_scales, 4))
+    return ZPP_ERR_MISALIGNED;
+  // one receiver (N = 1, l = 0) whose sources are the received chunks, `chunk` apart
+  return from_cuda(zpp::launch_dequant_reduce_requant(codes, scales, chunk, chunk, block, bits, 1,
+                                                      sources, 0, 1, out_codes, out_scales,
+                                                      stream));
+}
+
+zpp_status zpp_dequant_reduce_local(const void* codes, const float* scales, int64_t slice,
+                                    int32_t block, int32_t bits, int32_t sources,
+                                    float post_scale, void* out, zpp_dtype out_dt,
+                                    cudaStream_t stream) {
+  const zpp_status st = check_received(slice, block, bits, sources);
+  if (st != ZPP_OK) return st;
+  if (out_dt != ZPP_F16 && out_dt != ZPP_BF16 && out_dt != ZPP_F32) return ZPP_ERR_INVALID_ARG;
+  if (!(post_scale == post_scale) || post_scale - post_scale != 0.0f) return ZPP_ERR_INVALID_ARG;
+  if (slice == 0) return ZPP_OK;
+  if (!codes || !scales || !out) return ZPP_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(out, 16) || !aligned(scales, 4)) return ZPP_ERR_MISALIGNED;
+  // one receiver (n = 0, l = 0) whose N sources are the received slices, `slice` apart
+  return from_cuda(zpp::launch_dequant_reduce(codes, scales, slice, slice, block, bits, sources, 1,
+                                              0, 1, 1, post_scale, out, static_cast<int>(out_dt),
+                                              stream));
 }
 
 zpp_status zpp_device_fault(uint32_t* flags, int32_t clear) {

@@ -17,10 +17,11 @@ cudaError_t launch_dequant(const void* codes, const float* scales, int64_t n, in
 
 // The qgZ launchers cover the hop-1 chunks / receivers with local index l in
 // [l_begin, l_end) (the whole exchange is [0, M)).
-// K3: slice reorder + block quantisation of W = N*M ranks of E elements.
+// K3: slice reorder + block quantisation of `ranks` consecutive ranks of E elements each
+// (all W = N*M ranks of the virtual layout, or the one rank of a real device).
 cudaError_t launch_reorder_quant(const void* grads, int is_bf16, int64_t E, int block, int bits,
-                                 int N, int M, int l_begin, int l_end, void* codes, float* scales,
-                                 cudaStream_t s);
+                                 int N, int M, int l_begin, int l_end, int ranks, void* codes,
+                                 float* scales, cudaStream_t s);
 
 // K3 over a bucket given as tensors (the flatten fused in; whole exchange only). Tensor t
 // holds the W ranks' copies back to back, rank r's at ptr[t] + r * len_t, len_t =
@@ -43,17 +44,24 @@ cudaError_t launch_reorder_quant_tensors_bf16(const TensorTable& tab, int64_t E,
                                               int bits, int N, int M, bool v8, void* codes,
                                               float* scales, cudaStream_t s);
 
-// K4: intra-node fused dequantise -> fp32 sum over M chunks -> requantise.
+// K4: intra-node fused dequantise -> fp32 sum over M sources -> requantise. Receiver
+// (n, l), n < N, reads C elements at offset l*C of sources n*M .. n*M+M-1, which lie E
+// elements apart, and writes C codes at receiver offset (n*M + l)*C. The virtual layout
+// has C = E / M; one real rank's received chunks are N = 1, l = 0 and E = C.
 cudaError_t launch_dequant_reduce_requant(const void* codes, const float* scales, int64_t E,
-                                          int block, int bits, int N, int M, int l_begin,
-                                          int l_end, void* out_codes, float* out_scales,
-                                          cudaStream_t s);
+                                          int64_t C, int block, int bits, int N, int M,
+                                          int l_begin, int l_end, void* out_codes,
+                                          float* out_scales, cudaStream_t s);
 
 // K5: inter-node dequantise -> fp32 sum over N slices, times post_scale, stored as fp16
-// (out_kind 0), bf16 (1) or fp32 (2).
-cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t E, int block,
-                                  int bits, int N, int M, int l_begin, int l_end, float post_scale,
-                                  void* out, int out_kind, cudaStream_t s);
+// (out_kind 0), bf16 (1) or fp32 (2). Receiver (n, l), n < nz, reads S elements at offset
+// n*S of the N hop-1 outputs of ranks (n', l), which are C elements long and M outputs
+// apart, and writes S outputs at (n*M + l)*S. The virtual layout has S = E / W, C = E / M,
+// nz = N; one real rank's received slices are S = C, M = 1, nz = 1, l = 0.
+cudaError_t launch_dequant_reduce(const void* codes, const float* scales, int64_t S, int64_t C,
+                                  int block, int bits, int N, int M, int l_begin, int l_end,
+                                  int nz, float post_scale, void* out, int out_kind,
+                                  cudaStream_t s);
 
 // The device fault word: bits set by kernels whose bounded waits ran out (1: a producer
 // wait of the INT8 K4 ring, 2: a consumer wait of that ring, 4: the wait self-test).

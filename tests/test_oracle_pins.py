@@ -531,3 +531,66 @@ def test_averaged_two_hop_result_within_bound():
                       oracle.BF16).astype(np.float64)
     half_ulp = np.abs(a16) * 2.0 ** -8
     assert np.all(np.abs(a16 - direct) <= bound + U * np.abs(avg) + half_ulp)
+
+
+# --------------------------------------------------------------------------- received chunks
+def _received(c0, s0, c1, s1, N, M, E, block, bits, r):
+    """The buffers rank r receives in the two hops of the virtual layout: chunk l of its
+    node's ranks (local-index order), then slice n of the hop-1 outputs of ranks (n', l)."""
+    W, C, S = N * M, E // M, E // (N * M)
+    n, l = divmod(r, M)
+    cbC, cbS = oracle.code_bytes(C, bits), oracle.code_bytes(S, bits)
+    h1c = np.stack([c0[n * M + j][l * cbC:(l + 1) * cbC] for j in range(M)])
+    h1s = np.stack([s0[n * M + j][l * (C // block):(l + 1) * (C // block)] for j in range(M)])
+    h2c = np.stack([c1[j * M + l][n * cbS:(n + 1) * cbS] for j in range(N)])
+    h2s = np.stack([s1[j * M + l][n * (S // block):(n + 1) * (S // block)] for j in range(N)])
+    return h1c, h1s, h2c, h2s
+
+
+@pytest.mark.parametrize("N,M", [(1, 2), (2, 2), (2, 4), (3, 2), (1, 3), (4, 1)])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_one_receivers_hops_equal_its_row_of_the_exchange(N, M, bits):
+    """The per-receiver hop functions, fed the chunks / slices the exchange delivers, give
+    the receiver's row of the whole-exchange functions (which are pinned above by
+    placement, error bounds and the fixture): the index maps of the two formulations agree."""
+    W, block = N * M, 64
+    E = W * 3 * block
+    g = inputs.draw("laplace", W * E, seed=70 + W + bits, dtype=torch.bfloat16).reshape(W, E)
+    c0, s0, c1, s1, out = oracle.qgz_pipeline(bits16(g), oracle.BF16, block, bits, N, M)
+    avg = oracle.dequant_reduce_scaled(c1, s1, E, block, bits, N, M, 1.0 / W, oracle.BF16)
+    for r in range(W):
+        h1c, h1s, h2c, h2s = _received(c0, s0, c1, s1, N, M, E, block, bits, r)
+        oc, os_ = oracle.dequant_reduce_requant_chunks(h1c, h1s, E // M, block, bits)
+        assert np.array_equal(oc, c1[r]) and np.array_equal(os_.view(np.uint32),
+                                                            s1[r].view(np.uint32))
+        f = oracle.dequant_reduce_chunks(h2c, h2s, E // W, block, bits)
+        assert np.array_equal(f.view(np.uint32), out[r].view(np.uint32))
+        fa = oracle.dequant_reduce_chunks(h2c, h2s, E // W, block, bits, 1.0 / W, oracle.BF16)
+        assert np.array_equal(fa, avg[r])
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_one_chunk_reduces_to_its_dequantisation(bits):
+    """With one source the hop-2 sum is fma(q, s, +0) = fl32(q * s), the dequantisation."""
+    x = inputs.draw("uniform_outliers", 4 * 256, seed=5, dtype=torch.float16)
+    codes, scales = oracle.quant_blockwise(bits16(x), oracle.F16, 256, bits)
+    got = oracle.dequant_reduce_chunks(codes[None], scales[None], x.numel(), 256, bits)
+    want = oracle.dequant_blockwise(codes, scales, x.numel(), 256, bits, oracle.F32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("K", [2, 4, 8])
+def test_identical_exact_chunks_sum_exactly(K):
+    """K identical chunks whose terms are exact small multiples of a power-of-two scale:
+    every sum is K times the term exactly, and the requantised block keeps the codes with
+    K times the scale."""
+    block, bits = 64, 4
+    q = np.tile(np.array([7, -7, 3, 0, -1, 5, 2, -4], np.int64), 2 * block // 8)
+    nib = (q & 0xF).astype(np.uint8)
+    codes = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)
+    scales = np.full(2, 2.0 ** -10, np.float32)
+    ch = np.stack([codes] * K), np.stack([scales] * K)
+    total = oracle.dequant_reduce_chunks(*ch, 2 * block, block, bits)
+    assert np.array_equal(total, (K * q * 2.0 ** -10).astype(np.float32))
+    oc, os_ = oracle.dequant_reduce_requant_chunks(*ch, 2 * block, block, bits)
+    assert np.array_equal(oc, codes) and np.all(os_ == np.float32(K * 2.0 ** -10))

@@ -517,3 +517,79 @@ def test_device_copy():
     zpp.device_copy(a, b)
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------- one real rank's calls
+@pytest.mark.parametrize("N,M", [(1, 1), (2, 2), (2, 4), (3, 2), (4, 3), (1, 16), (2, 6), (4, 8)])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_local_calls_equal_the_ranks_row(N, M, bits):
+    """The calls a real rank makes on its own buffers: step 1 on its bucket (whole and chunk
+    by chunk), the fused hop on the chunks it receives, the final hop on the slices it
+    receives -- each against the oracle, which gives the rank's row of the exchange."""
+    from tests.test_oracle_pins import _received
+    W = N * M
+    for block, per_slice in ((64, 2 * 64), (512, 3 * 8192 + 512)):
+        if W * W * per_slice > (1 << 23):
+            per_slice = 2 * block
+        E = W * per_slice
+        g = inputs.draw("laplace", W * E, seed=3 * W + bits + block, dtype=torch.bfloat16,
+                        device=DEV).reshape(W, E)
+        c0, s0, c1, s1, out = oracle.qgz_pipeline(bits16(g), oracle.BF16, block, bits, N, M)
+        for r in sorted({0, W - 1, W // 2}):
+            lc, ls = zpp.qgz_reorder_quant_local(g[r], block, bits, N, M)
+            assert np.array_equal(host(lc), c0[r]) and np.array_equal(host(ls), s0[r])
+            pc = torch.full_like(lc, 0x5A)
+            ps = torch.full_like(ls, -1.0)
+            for p in range(M):
+                zpp.qgz_reorder_quant_local(g[r], block, bits, N, M, pc, ps, chunks=(p, p + 1))
+            assert torch.equal(pc, lc) and torch.equal(ps.view(torch.int32), ls.view(torch.int32))
+            h1c, h1s, h2c, h2s = (torch.from_numpy(a).to(DEV) for a in
+                                  _received(c0, s0, c1, s1, N, M, E, block, bits, r))
+            oc, os_ = zpp.dequant_reduce_requant_local(h1c, h1s, E // M, block, bits, M)
+            assert np.array_equal(host(oc), c1[r])
+            assert np.array_equal(host(os_).view(np.uint32), s1[r].view(np.uint32))
+            f = zpp.dequant_reduce_local(h2c, h2s, E // W, block, bits, N)
+            assert_f32_parity(host(f), out[r])
+            fa = zpp.dequant_reduce_local(h2c, h2s, E // W, block, bits, N, post_scale=1.0 / W,
+                                          dtype=torch.bfloat16)
+            want = oracle.dequant_reduce_chunks(h2c.cpu().numpy(), h2s.cpu().numpy(), E // W,
+                                                block, bits, 1.0 / W, oracle.BF16)
+            assert np.array_equal(bits16(fa), want)
+    assert zb.zpp_device_fault() == 0
+
+
+def _one_rank_exchange(port, q):
+    import os
+    import traceback
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    try:
+        import torch.distributed as dist
+        from quantized_zero_communication_gb300 import exchange
+        torch.cuda.set_device(0)
+        dist.init_process_group("nccl", rank=0, world_size=1)
+        groups = exchange.Groups(1, 1)
+        g = inputs.draw("laplace", 8192, seed=2, dtype=torch.bfloat16, device="cuda:0")
+        res = [exchange.qgz_step(g, 256, 4, groups, pipelined=p).cpu().numpy() for p in (0, 1)]
+        dist.destroy_process_group()
+        want = oracle.qgz_pipeline(bits16(g)[None], oracle.BF16, 256, 4, 1, 1)[4][0]
+        ok = all(np.array_equal(r.view(np.uint32), want.view(np.uint32)) for r in res)
+        q.put("ok" if ok else "owner slice differs from the oracle")
+    except Exception:
+        q.put(traceback.format_exc())
+
+
+def test_exchange_step_on_one_nccl_rank():
+    """The real-rank qgZ step (local kernels + NCCL collectives) on a world of one: both the
+    all-to-all and the point-to-point hop-1 forms give the oracle's owner slice."""
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_one_rank_exchange, args=(port, q))
+    p.start()
+    msg = q.get(timeout=300)
+    p.join(60)
+    assert msg == "ok", msg
