@@ -734,8 +734,9 @@ def run_reference(args):
 def run_sweep(args):
     """Times K1, K2 and the fused K-way hop (topology 1 x K, K in {2, 8, 16}) over the
     sweep's sizes x dtypes x bits x blocks (N(0, 0.02) data; timing does not depend on the
-    values), 20 event-timed launches each after 3 warm-up ones; sizes whose buffers fit in
-    the 129 MB L2 are flushed by a 256 MiB write between launches."""
+    values): 20 launches after 3 warm-up ones, back to back between one pair of events when
+    the buffers exceed the 129 MB L2, else one by one with a 256 MiB write flushing L2
+    before each."""
     import torch
     import quantized_zero_communication_gb300 as zpp
     from quantized_zero_communication_gb300 import build as zbuild, inputs
@@ -750,10 +751,18 @@ def run_sweep(args):
     def timed(fn, small):
         for _ in range(3):
             fn()
+        if not small:  # buffers larger than L2: 20 launches back to back, one event pair
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / 20 * 1e-3
         tot = 0.0
         for _ in range(20):
-            if small:
-                flush.fill_(1)
+            flush.fill_(1)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()
@@ -762,12 +771,17 @@ def run_sweep(args):
             tot += a.elapsed_time(b)
         return tot / 20 * 1e-3
 
+    def pick(values, chosen):
+        return [v for v in values if not chosen or v in chosen]
+
+    dtypes = [d for d in inputs.SWEEP_DTYPES
+              if not args.sweep_dtypes or str(d).replace("torch.", "") in args.sweep_dtypes]
     rows = []
-    for size in inputs.SWEEP_SIZES:
-        for dt in inputs.SWEEP_DTYPES:
+    for size in pick(inputs.SWEEP_SIZES, [1 << e for e in args.sweep_log2 or []]):
+        for dt in dtypes:
             x = inputs.draw("normal", size, seed=100, dtype=dt, device=dev)
-            for bits in inputs.SWEEP_BITS:
-                for block in inputs.SWEEP_BLOCKS:
+            for bits in pick(inputs.SWEEP_BITS, args.sweep_bits):
+                for block in pick(inputs.SWEEP_BLOCKS, args.sweep_blocks):
                     cb, ns = code_bytes(size, bits), math.ceil(size / block)
                     codes, scales = zpp.quant_blockwise(x, block, bits)
                     y = torch.empty_like(x)
@@ -781,7 +795,7 @@ def run_sweep(args):
                            "quant_us": round(t1 * 1e6, 1), "quant_frac": round(b12 / t1 / 1e9 / peak, 3),
                            "dequant_us": round(t2 * 1e6, 1), "dequant_frac": round(b12 / t2 / 1e9 / peak, 3)}
                     if dt == torch.bfloat16:
-                        for K in (2, 8, 16):
+                        for K in pick((2, 8, 16), args.sweep_k):
                             E = size // K
                             if E % (K * block):
                                 continue
@@ -811,6 +825,12 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="time quant, dequant and the fused hop over the sweep's sizes, dtypes, "
                          "widths and blocks (one JSON object; not the benchmark line)")
+    ap.add_argument("--sweep-log2", type=int, nargs="*",
+                    help="with --sweep: only these sizes (log2 of the element count)")
+    ap.add_argument("--sweep-bits", type=int, nargs="*", help="with --sweep: only these widths")
+    ap.add_argument("--sweep-blocks", type=int, nargs="*", help="with --sweep: only these blocks")
+    ap.add_argument("--sweep-dtypes", nargs="*", help="with --sweep: float16 and/or bfloat16")
+    ap.add_argument("--sweep-k", type=int, nargs="*", help="with --sweep: fused-hop K values")
     ap.add_argument("--only", choices=("K1", "K2", "K3", "K4", "K5"),
                     help="time one kernel of the step on the full workload, keeping only its "
                          "own buffers on the device (profiling runs)")

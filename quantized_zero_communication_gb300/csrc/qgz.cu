@@ -27,12 +27,13 @@ namespace zpp {
 // in K5; a CTA tile is 8 warps x one row.
 //
 // K4 kernels, chosen per launch by drr_bits / run_drr (all give the same bits):
-//   k_dequant_reduce_requant_ring8<KC>          INT8 codes, any M: the bulk-copy ring below;
-//   k_dequant_reduce_requant_staged<4, KC, SPLIT>  INT4, M = KC in {2, 4, 8} or M = 16: the
-//       full CTA tiles, the sources' codes staged in shared memory by cp.async;
+//   k_dequant_reduce_requant_ring8<KC>          INT8 codes, M >= 3: the bulk-copy ring below;
+//   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  INT4 with M = KC in {2, 4, 8} or
+//       M = 16, INT8 with M = 2: the full CTA tiles, the sources' codes staged in shared
+//       memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<4, KC, EXACT>      INT4 otherwise: M = 1, M not a multiple of
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   otherwise: M = 1, INT4 M not a multiple of
 //       its chunk, and the ragged last tile of a 2-source staged launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
@@ -285,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
 }
 
 // ---------------------------------------------------------------------------------
-// K4 for INT8 codes: a bulk-copy ring. One CTA per SM; 16 consumer warps and one producer
+// K4 for INT8 codes and 3 or more sources: a bulk-copy ring. One CTA per SM; 16 consumer
+// warps and one producer
 // warp. A unit is 8192 consecutive outputs of one receiver (16 warps x 32 lanes x 16
 // codes); the units are dealt to the CTAs round robin. The producer streams each unit's
 // sources, KC at a time, into a ring of NS shared-memory stages with cp.async.bulk (one
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     k_dequant_reduce_requant_ring8(const uint8_t* __restrict__ codes,
                                    const float* __restrict__ scales, int64_t E, int64_t C,
                                    int log2b, int N, int M, int l_begin, int l_end,
-                                   uint8_t* __restrict__ out_codes,
+                                   bool scales_bulk, uint8_t* __restrict__ out_codes,
                                    float* __restrict__ out_scales) {
   using G = RingGeo<KC>;
   constexpr int NS = G::STAGES;
@@ -373,25 +375,34 @@ __global__ void __launch_bounds__(kRingThreads, 1)
       const uint8_t* csrc = codes + static_cast<int64_t>(n) * M * cb_in + idx;
       const float* ssrc = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
       const int nsc = valid >> log2b;  // whole blocks: C and e0 are multiples of the block
+      // the unit's scales of one source: one bulk copy when they span whole 16-byte
+      // groups at 16-byte aligned addresses, else one 4-byte copy each
+      const bool bulk_sc = scales_bulk && (nsc & 3) == 0;
       for (int g = 0; g < groups; ++g) {
         if (!mbar_try_wait(&empty[s], phase) && !mbar_wait_bounded(&empty[s], phase, kRingWaitNs)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], static_cast<unsigned>(valid) * KC);
+          mbar_arrive_expect_tx(&full[s], (static_cast<unsigned>(valid) +
+                                           (bulk_sc ? 4u * nsc : 0u)) * KC);
 #pragma unroll
-          for (int i = 0; i < KC; ++i)
+          for (int i = 0; i < KC; ++i) {
             bulk_load(st_codes + (s * KC + i) * kRingSrcBytes,
                       csrc + static_cast<int64_t>(g * KC + i) * cb_in, static_cast<unsigned>(valid),
                       &full[s]);
+            if (bulk_sc)
+              bulk_load(st_scales + (s * KC + i) * kRingScaleSlots,
+                        ssrc + static_cast<int64_t>(g * KC + i) * sc_in, 4u * nsc, &full[s]);
+          }
         }
-        for (int j = lane; j < KC * nsc; j += 32) {
-          const int i = j / nsc, b = j - i * nsc;
-          cp_async4(st_scales + (s * KC + i) * kRingScaleSlots + b,
-                    ssrc + static_cast<int64_t>(g * KC + i) * sc_in + b);
-        }
-        cp_async_arrive_noinc(&full[s]);
+        if (!bulk_sc)
+          for (int j = lane; j < KC * nsc; j += 32) {
+            const int i = j / nsc, b = j - i * nsc;
+            cp_async4(st_scales + (s * KC + i) * kRingScaleSlots + b,
+                      ssrc + static_cast<int64_t>(g * KC + i) * sc_in + b);
+          }
+        cp_async_arrive_noinc(&full[s]);  // counts even with no copies of its own
         ++issued;
         if (++s == NS) s = 0, phase ^= 1u;
       }
@@ -623,29 +634,50 @@ static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, 
                             float* out_scales, cudaStream_t s) {
   auto kern = k_dequant_reduce_requant_ring8<KC>;
   constexpr int smem = RingGeo<KC>::SMEM;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // per-device set-up, done once: the dynamic shared-memory limit and the SM count
+  constexpr int kMaxDevices = 64;
+  static int sms_of[kMaxDevices];  // 0: not set up yet
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  int dev = 0, sms = 0;
-  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return err;
+  int sms = dev < kMaxDevices ? sms_of[dev] : 0;
+  if (sms == 0) {
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+        cudaSuccess)
+      return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return err;
+    if (dev < kMaxDevices) sms_of[dev] = sms;
+  }
   const int64_t T = (C + kRingTile - 1) / kRingTile;
   const int64_t U = static_cast<int64_t>(N) * (le - lb) * T;
   const unsigned grid = static_cast<unsigned>(U < sms ? U : sms);
+  // scale rows start on 16-byte boundaries: per-source stride, chunk offsets and unit
+  // offsets all whole groups of 4 scales, and the array itself 16-byte aligned
+  const int64_t sc_in = E >> log2b;
+  const bool scales_bulk = (reinterpret_cast<uintptr_t>(scales) & 15) == 0 && sc_in % 4 == 0 &&
+                           (C >> log2b) % 4 == 0 && (kRingTile >> log2b) % 4 == 0;
   kern<<<grid, kRingThreads, smem, s>>>(static_cast<const uint8_t*>(codes), scales, E, C, log2b,
-                                        N, M, lb, le, static_cast<uint8_t*>(out_codes),
-                                        out_scales);
+                                        N, M, lb, le, scales_bulk,
+                                        static_cast<uint8_t*>(out_codes), out_scales);
   return cudaGetLastError();
 }
 
 template <int BITS>
 static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int64_t C, int log2b, int N,
                             int M, int lb, int le, void* oc, float* os, cudaStream_t s) {
-  if constexpr (BITS == 8) {  // the bulk-copy ring, for any M (sources in groups of KC)
-    if (M % 8 == 0) return run_ring8<8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-    if (M % 4 == 0) return run_ring8<4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-    if (M % 2 == 0) return run_ring8<2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-    return run_ring8<1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+  // INT8 with 3 or more sources: the bulk-copy ring (sources in groups of KC). With one or
+  // two sources the requantisation dominates and the 32 warps per SM of the per-CTA kernels
+  // hide its latency better (2^30 codes, K = 2: 389 us staged against 489 us in the ring).
+  if constexpr (BITS == 8) {
+    if (M > 2) {
+      if (M % 8 == 0) return run_ring8<8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      if (M % 4 == 0) return run_ring8<4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      if (M % 2 == 0) return run_ring8<2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      return run_ring8<1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    }
+    if (M == 2) return run_drr<BITS, 2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    return run_drr<BITS, 1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
   } else {
     switch (chunk_for(M)) {
       case 8: return run_drr<BITS, 8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
