@@ -24,7 +24,7 @@
 namespace zpp {
 
 // Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
-// in K5; a CTA tile is 8 warps x one row.
+// in K5; a CTA tile is 8 warps x one row (4 warps in the INT4 staged kernel).
 //
 // K4 kernels, chosen per launch by drr_bits / run_drr (all give the same bits):
 //   k_dequant_reduce_requant_ring8<KC>          INT8 codes, M >= 3: the bulk-copy ring below;
@@ -232,32 +232,43 @@ __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
                                      out_scales);
 }
 
-template <int KC>
-constexpr int staged_smem_bytes() { return KC * kThreads * 16; }
+// CTA of the staged kernel: 4 warps for INT4 codes (a 4096-code block is 4 rows, so every
+// block fits one CTA), 8 for INT8 (8 rows of 512). Measured on GB300 (4 x 8 bucket, INT4,
+// 8 sources): 65.8 us with CTAs of 1, 2 or 4 warps against 67.6 us with 8.
+template <int BITS>
+constexpr int staged_warps() { return BITS == 4 ? 4 : 8; }
+template <int BITS, int KC>
+constexpr int staged_smem_bytes() { return KC * staged_warps<BITS>() * 32 * 16; }
+// CTAs per SM at 64 registers; 16 sources (32 KB of stage per 4-warp CTA): 6 CTAs per SM
+template <int BITS, int KC>
+constexpr int staged_min_ctas() {
+  return KC > 8 ? 3 * 8 / staged_warps<BITS>() : kStagedMinCtas * 8 / staged_warps<BITS>();
+}
 
-// K4, exactly KC (2, 4, 8 or 16) sources per receiver, full CTA tiles only: every thread
+// K4, exactly KC (2, 4, 8 or 16) sources per receiver, full tiles only: every thread
 // stages its 16 code bytes of each source (32 INT4 or 16 INT8 codes) in shared memory with
-// cp.async (the copies do not occupy registers, so 4 CTAs fit per SM), in two commit
-// groups; the first half of the sources is reduced while the second half is still landing. Each thread reads back only
+// cp.async (the copies do not occupy registers), in two commit groups; the first half of
+// the sources is reduced while the second half is still landing. Each thread reads back only
 // the slots it filled, and every slot is written once per launch, so no barrier is needed.
 // Measured on GB300 (4 x 8 bucket) 68 us against 72 us for the same tile with the codes
-// held in registers at 3 CTAs per SM. With 16 sources the stage is 64 KB (3 CTAs per SM).
+// held in registers at 3 CTAs per SM. Grid x counts CTA tiles of staged_warps rows.
 template <int BITS, int KC, int SPLIT>
-__global__ void __launch_bounds__(kThreads, KC > 8 ? 3 : kStagedMinCtas)
+__global__ void __launch_bounds__(staged_warps<BITS>() * 32, staged_min_ctas<BITS, KC>())
     k_dequant_reduce_requant_staged(const uint8_t* __restrict__ codes,
                                     const float* __restrict__ scales, int64_t E, int64_t C,
                                     int log2b, int l_begin, uint8_t* __restrict__ out_codes,
                                     float* __restrict__ out_scales) {
   using G = Geo4<BITS>;
-  constexpr int M = KC, H = KC / 2;
-  extern __shared__ uint4 stage_mem[];  // [KC][kThreads], staged_smem_bytes<KC>()
-  uint4(*stage)[kThreads] = reinterpret_cast<uint4(*)[kThreads]>(stage_mem);
+  constexpr int M = KC, H = KC / 2, NT = staged_warps<BITS>() * 32;
+  extern __shared__ uint4 stage_mem[];  // [KC][NT], staged_smem_bytes<BITS, KC>()
+  uint4(*stage)[NT] = reinterpret_cast<uint4(*)[NT]>(stage_mem);
   __shared__ float red[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
   const int64_t r = static_cast<int64_t>(n) * M + l;
   const int64_t cb_in = E * BITS / 8, sc_in = E >> log2b;
-  const int64_t e = static_cast<int64_t>(blockIdx.x) * G::CTA + warp * G::ROW + lane * G::EPL;
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * (NT / 32 * G::ROW) + warp * G::ROW +
+                    lane * G::EPL;
   const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
   const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx * BITS / 8;
   const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
@@ -536,19 +547,21 @@ __global__ void __launch_bounds__(kThreads)
 
 static int chunk_for(int k) { return k >= 8 ? 8 : (k > 2 ? 4 : (k == 2 ? 2 : 1)); }
 
+// `full`: the number of whole 8-warp tiles (Geo4<BITS>::CTA outputs) per receiver
 template <int BITS, int KC, int SPLIT>
 static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, int64_t C,
                               int log2b, int lb, int64_t full, unsigned ny, unsigned nz,
                               uint8_t* oc, float* out_scales, cudaStream_t s) {
-  constexpr int smem = staged_smem_bytes<KC>();
+  constexpr int smem = staged_smem_bytes<BITS, KC>();
+  constexpr int NW = staged_warps<BITS>();
   auto kern = k_dequant_reduce_requant_staged<BITS, KC, SPLIT>;
   if constexpr (smem > 48 * 1024) {  // above the default dynamic shared-memory limit
     const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<dim3(static_cast<unsigned>(full), ny, nz), kThreads, smem, s>>>(c, scales, E, C, log2b,
-                                                                        lb, oc, out_scales);
+  kern<<<dim3(static_cast<unsigned>(full * (kWarps / NW)), ny, nz), NW * 32, smem, s>>>(
+      c, scales, E, C, log2b, lb, oc, out_scales);
   return cudaGetLastError();
 }
 
