@@ -28,13 +28,15 @@ namespace zpp {
 //
 // K4 kernels, chosen per launch by drr_bits / run_drr (all give the same bits):
 //   k_dequant_reduce_requant_ring8<KC>          INT8 codes, M >= 3: the bulk-copy ring below;
+//   k_dequant_reduce_requant_wide8<KC, V8>      INT8 codes, M = 1 or 2: the full tiles, 32
+//       outputs per lane, the codes loaded straight into registers;
 //   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  INT4 with M = KC in {2, 4, 8} or
-//       M = 16, INT8 with M = 2: the full CTA tiles, the sources' codes staged in shared
-//       memory by cp.async;
+//       M = 16: the full tiles, the sources' codes staged in shared memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<BITS, KC, EXACT>   otherwise: M = 1, INT4 M not a multiple of
-//       its chunk, and the ragged last tile of a 2-source staged launch.
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   otherwise: INT4 with M = 1 or M not a
+//       multiple of its chunk, and the ragged last tile of a 2-source staged launch or of
+//       a wide launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
@@ -116,30 +118,32 @@ __device__ __forceinline__ void reduce_sources(f32x2* acc, const uint8_t* cbase,
   }
 }
 
-// The end of a K4 tile: block absmax of the lane's sums (across lanes, and across warps
-// through `red` for blocks wider than a row), block scale, codes, and the stores at the
-// receiver's output offsets (codes at byte out_c + e*BITS/8, scales at out_s + e/B).
-template <int BITS, int SPLIT>
+// The end of a K4 tile: block absmax of the lane's EPL sums (across lanes, and across warps
+// through `red` for blocks wider than a row of 32 * EPL), block scale, codes, and the stores
+// at the receiver's output offsets (codes at byte out_c + e*BITS/8, scales at out_s + e/B).
+// A lane's codes are 4 words (st_v4) or 8 words (32 bytes: one 256-bit store when V8).
+template <int BITS, int SPLIT, int EPL = Geo4<BITS>::EPL, bool V8 = false>
 __device__ __forceinline__ void requant_store(const f32x2* acc, int lane, int warp, int B,
                                               int64_t e, bool valid, int64_t out_c,
                                               int64_t out_s, uint8_t* __restrict__ out_codes,
                                               float* __restrict__ out_scales, float* red) {
-  using G = Geo4<BITS>;
+  constexpr int NP = EPL / 2, ROW = 32 * EPL, NWORD = EPL * BITS / 32;
+  static_assert(NWORD == 4 || NWORD == 8, "a lane stores 16 or 32 code bytes");
   const int log2b = __ffs(B) - 1;
   float m = 0.0f;
 #pragma unroll
-  for (int j = 0; j < G::NP; ++j) {
+  for (int j = 0; j < NP; ++j) {
     float a, b;
     f2_split(acc[j], a, b);
     m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
   }
-  if (B <= G::ROW) {
-    m = warp_max(m, B / G::EPL);
+  if (B <= ROW) {
+    m = warp_max(m, B / EPL);
   } else {
     m = warp_max(m, 32);
     if (lane == 0) red[warp] = m;
     __syncthreads();
-    const int wpb = B / G::ROW, w0 = warp & ~(wpb - 1);
+    const int wpb = B / ROW, w0 = warp & ~(wpb - 1);
     m = red[w0];
     for (int i = 1; i < wpb; ++i) m = fmaxf(m, red[w0 + i]);
   }
@@ -147,19 +151,23 @@ __device__ __forceinline__ void requant_store(const f32x2* acc, int lane, int wa
   block_scale<BITS>(m, sc, iv);
   if (!valid) return;
   const f32x2 iv2 = f2(iv, iv);
-  uint32_t w[4];
+  U8x32 w;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < NWORD; ++k) {
     if constexpr (BITS == 8) {
       const f32x2 q[2] = {round_codes(acc[2 * k], iv2), round_codes(acc[2 * k + 1], iv2)};
-      w[k] = pack_int8x4(q);
+      w.w[k] = pack_int8x4(q);
     } else {
       const f32x2 q[4] = {round_codes(acc[4 * k], iv2), round_codes(acc[4 * k + 1], iv2),
                           round_codes(acc[4 * k + 2], iv2), round_codes(acc[4 * k + 3], iv2)};
-      w[k] = k < SPLIT ? pack_int4x8_eo(q) : pack_int4x8(q);
+      w.w[k] = k < SPLIT ? pack_int4x8_eo(q) : pack_int4x8(q);
     }
   }
-  st_v4(out_codes + out_c + e * BITS / 8, make_uint4(w[0], w[1], w[2], w[3]));
+  uint8_t* dst = out_codes + out_c + e * BITS / 8;
+  if constexpr (NWORD == 4)
+    st_v4(dst, make_uint4(w.w[0], w.w[1], w.w[2], w.w[3]));
+  else
+    st_vec32<V8>(dst, w);
   if ((e & (B - 1)) == 0) out_scales[out_s + (e >> log2b)] = sc;
 }
 
@@ -294,6 +302,48 @@ __global__ void __launch_bounds__(staged_warps<BITS>() * 32, staged_min_ctas<BIT
   }
   requant_store<BITS, SPLIT>(acc, lane, warp, 1 << log2b, e, true, r * (C * BITS / 8),
                              r * (C >> log2b), out_codes, out_scales, red);
+}
+
+// K4 for INT8 codes and exactly KC (1 or 2) sources, whole tiles of 4096 outputs: CTAs of
+// 4 warps (a 4096-code block is 4 rows), 32 outputs per lane; each source's 32 code bytes go
+// straight into registers (one 256-bit load when the buffers are 32-byte aligned, V8, else
+// two 128-bit loads), so a lane's requantisation is spread over twice the outputs of the
+// 16-code lanes. Measured on GB300 (topology 1 x 2, 2^28 / 2^30 codes, blocks 64-4096):
+// 0.87-0.94 / 0.94-1.01 of the measured copy bandwidth, against 0.57-0.66 / 0.61-0.70 for
+// the staged kernel with 16 outputs per lane and 0.67-0.74 for 32 outputs per lane staged
+// by two 16-byte cp.async per source.
+constexpr int kWide8Warps = 4;
+constexpr int kWide8Tile = kWide8Warps * 32 * 32;  // 4096 outputs, = Geo4<8>::CTA
+
+template <int KC, bool V8>
+__global__ void __launch_bounds__(kWide8Warps * 32, 8)
+    k_dequant_reduce_requant_wide8(const uint8_t* __restrict__ codes,
+                                   const float* __restrict__ scales, int64_t E, int64_t C,
+                                   int log2b, int l_begin, uint8_t* __restrict__ out_codes,
+                                   float* __restrict__ out_scales) {
+  constexpr int M = KC, EPL = 32, ROW = 32 * EPL;
+  __shared__ float red[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
+  const int64_t r = static_cast<int64_t>(n) * M + l;
+  const int64_t cb_in = E, sc_in = E >> log2b;
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * kWide8Tile + warp * ROW + lane * EPL;
+  const int64_t idx = static_cast<int64_t>(l) * C + e;  // chunk l of each source
+  const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx;
+  const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in + (idx >> log2b);
+  U8x32 v[KC];
+#pragma unroll
+  for (int i = 0; i < KC; ++i) v[i] = ld_vec32<V8>(cbase + i * cb_in);
+  float s[KC];
+#pragma unroll
+  for (int i = 0; i < KC; ++i) s[i] = __ldg(sbase + i * sc_in);
+  f32x2 acc[EPL / 2];
+#pragma unroll
+  for (int j = 0; j < EPL / 2; ++j) acc[j] = f2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < KC; ++i) accumulate<8, 8, 0>(acc, v[i].w, s[i]);
+  requant_store<8, 0, EPL, V8>(acc, lane, warp, 1 << log2b, e, true, r * C, r * (C >> log2b),
+                               out_codes, out_scales, red);
 }
 
 // ---------------------------------------------------------------------------------
@@ -676,12 +726,45 @@ static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, 
   return cudaGetLastError();
 }
 
+// INT8, M = KC (1 or 2) sources: the whole 4096-output tiles through the wide kernel, a ragged
+// last tile through the register kernel at that tile offset.
+template <int KC>
+static cudaError_t run_wide8(const void* codes, const float* scales, int64_t E, int64_t C,
+                            int log2b, int N, int lb, int le, void* out_codes, float* out_scales,
+                            cudaStream_t s) {
+  static_assert(kWide8Tile == Geo4<8>::CTA, "the tail kernel's tile offset counts wide tiles");
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  uint8_t* oc = static_cast<uint8_t*>(out_codes);
+  const unsigned ny = static_cast<unsigned>(le - lb), nz = static_cast<unsigned>(N);
+  const int64_t full = C / kWide8Tile;
+  if (full > 0) {
+    // every lane's 32 code bytes start on a 32-byte boundary when both bases do (E and C
+    // are multiples of the block, so of 64)
+    const bool v8 = ((reinterpret_cast<uintptr_t>(codes) | reinterpret_cast<uintptr_t>(out_codes)) &
+                     31) == 0;
+    const dim3 grid(static_cast<unsigned>(full), ny, nz);
+    if (v8)
+      k_dequant_reduce_requant_wide8<KC, true><<<grid, kWide8Warps * 32, 0, s>>>(
+          c, scales, E, C, log2b, lb, oc, out_scales);
+    else
+      k_dequant_reduce_requant_wide8<KC, false><<<grid, kWide8Warps * 32, 0, s>>>(
+          c, scales, E, C, log2b, lb, oc, out_scales);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (C % kWide8Tile != 0)
+    k_dequant_reduce_requant<8, KC, true><<<dim3(1, ny, nz), kThreads, 0, s>>>(
+        c, scales, E, C, log2b, KC, lb, static_cast<int>(full), oc, out_scales);
+  return cudaGetLastError();
+}
+
 template <int BITS>
 static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int64_t C, int log2b, int N,
                             int M, int lb, int le, void* oc, float* os, cudaStream_t s) {
   // INT8 with 3 or more sources: the bulk-copy ring (sources in groups of KC). With one or
-  // two sources the requantisation dominates and the 32 warps per SM of the per-CTA kernels
-  // hide its latency better (2^30 codes, K = 2: 389 us staged against 489 us in the ring).
+  // two sources the requantisation dominates: the wide kernel (32 outputs per lane, codes
+  // in registers) spreads it over the most outputs (2^30 codes, K = 2: 246-251 us, against
+  // 389 us staged and 489 us in the ring).
   if constexpr (BITS == 8) {
     if (M > 2) {
       if (M % 8 == 0) return run_ring8<8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
@@ -689,8 +772,8 @@ static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int64_t C
       if (M % 2 == 0) return run_ring8<2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
       return run_ring8<1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
     }
-    if (M == 2) return run_drr<BITS, 2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-    return run_drr<BITS, 1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+    if (M == 2) return run_wide8<2>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
+    return run_wide8<1>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
   } else {
     switch (chunk_for(M)) {
       case 8: return run_drr<BITS, 8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
