@@ -30,13 +30,14 @@ namespace zpp {
 //   k_dequant_reduce_requant_ring8<KC>          INT8 codes, M >= 3: the bulk-copy ring below;
 //   k_dequant_reduce_requant_wide8<KC, V8>      INT8 codes, M = 1 or 2: the full tiles, 32
 //       outputs per lane, the codes loaded straight into registers;
-//   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  INT4 with M = KC in {2, 4, 8} or
+//   k_dequant_reduce_requant_prefetch<KC>       INT4 codes, M = 1 or 2: the full tiles, two
+//       per CTA, both loaded into registers before the first is converted;
+//   k_dequant_reduce_requant_staged<BITS, KC, SPLIT>  INT4 with M = KC in {4, 8} or
 //       M = 16: the full tiles, the sources' codes staged in shared memory by cp.async;
 //   k_dequant_reduce_requant_split<KC>          INT4, M a multiple of a 4- or 8-source
 //       chunk otherwise, and the ragged last tile of a staged launch;
-//   k_dequant_reduce_requant<BITS, KC, EXACT>   otherwise: INT4 with M = 1 or M not a
-//       multiple of its chunk, and the ragged last tile of a 2-source staged launch or of
-//       a wide launch.
+//   k_dequant_reduce_requant<BITS, KC, EXACT>   otherwise: INT4 with M not a multiple of
+//       its chunk, and the ragged last tile of a prefetching or a wide launch.
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
@@ -344,6 +345,59 @@ __global__ void __launch_bounds__(kWide8Warps * 32, 8)
   for (int i = 0; i < KC; ++i) accumulate<8, 8, 0>(acc, v[i].w, s[i]);
   requant_store<8, 0, EPL, V8>(acc, lane, warp, 1 << log2b, e, true, r * C, r * (C >> log2b),
                                out_codes, out_scales, red);
+}
+
+// K4 for INT4 codes and exactly KC (1 or 2) sources. With so few terms per output the
+// requantisation and the load latency dominate, so each CTA (4 warps) takes two tiles of
+// 4096 outputs and loads both tiles' codes (16 bytes per source per lane) into registers
+// before converting the first; every code word takes the split conversion. A CTA covers
+// one 8-warp tile of Geo4<4> (8192 outputs). Measured on GB300 (topology 1 x 2, 2^28 / 2^30
+// codes, blocks 64-4096): 0.58-0.68 / 0.63-0.74 of the measured copy bandwidth, against
+// 0.42-0.49 / 0.43-0.52 for the staged kernel (one tile per CTA); three or four tiles per
+// CTA measured no better than two.
+constexpr int kPrefetchWarps = 4;
+constexpr int kPrefetchTile = kPrefetchWarps * 1024;  // outputs per tile; two per CTA
+
+template <int KC>
+__global__ void __launch_bounds__(kPrefetchWarps * 32, 8)
+    k_dequant_reduce_requant_prefetch(const uint8_t* __restrict__ codes,
+                                      const float* __restrict__ scales, int64_t E, int64_t C,
+                                      int log2b, int l_begin, uint8_t* __restrict__ out_codes,
+                                      float* __restrict__ out_scales) {
+  using G = Geo4<4>;
+  constexpr int M = KC;
+  __shared__ float red[2][kWarps];  // one row per tile: blocks wider than a row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int l = l_begin + static_cast<int>(blockIdx.y), n = blockIdx.z;
+  const int64_t r = static_cast<int64_t>(n) * M + l;
+  const int64_t cb_in = E / 2, sc_in = E >> log2b;
+  const int64_t e0 =
+      static_cast<int64_t>(blockIdx.x) * (2 * kPrefetchTile) + warp * G::ROW + lane * G::EPL;
+  const int64_t idx0 = static_cast<int64_t>(l) * C + e0;  // chunk l of each source
+  const uint8_t* cbase = codes + static_cast<int64_t>(n) * M * cb_in + idx0 / 2;
+  const float* sbase = scales + static_cast<int64_t>(n) * M * sc_in;
+  uint4 v[2][KC];
+  float s[2][KC];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+      v[t][i] = ld_stream_v4(cbase + i * cb_in + t * (kPrefetchTile / 2));
+      s[t][i] = __ldg(sbase + i * sc_in + ((idx0 + t * kPrefetchTile) >> log2b));
+    }
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    f32x2 acc[G::NP];
+#pragma unroll
+    for (int j = 0; j < G::NP; ++j) acc[j] = f2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+      const uint32_t w[4] = {v[t][i].x, v[t][i].y, v[t][i].z, v[t][i].w};
+      accumulate<4, 4, 4>(acc, w, s[t][i]);
+    }
+    requant_store<4, 4>(acc, lane, warp, 1 << log2b, e0 + t * kPrefetchTile, true, r * (C / 2),
+                        r * (C >> log2b), out_codes, out_scales, red[t]);
+  }
 }
 
 // ---------------------------------------------------------------------------------
@@ -726,6 +780,30 @@ static cudaError_t run_ring8(const void* codes, const float* scales, int64_t E, 
   return cudaGetLastError();
 }
 
+// INT4, M = KC (1 or 2) sources: the whole 8192-output tiles through the prefetching kernel,
+// a ragged last tile through the register kernel at that tile offset.
+template <int KC>
+static cudaError_t run_prefetch(const void* codes, const float* scales, int64_t E, int64_t C,
+                               int log2b, int N, int lb, int le, void* out_codes,
+                               float* out_scales, cudaStream_t s) {
+  static_assert(2 * kPrefetchTile == Geo4<4>::CTA, "the tail kernel's tile offset counts CTAs");
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  uint8_t* oc = static_cast<uint8_t*>(out_codes);
+  const unsigned ny = static_cast<unsigned>(le - lb), nz = static_cast<unsigned>(N);
+  const int64_t full = C / Geo4<4>::CTA;
+  if (full > 0) {
+    k_dequant_reduce_requant_prefetch<KC>
+        <<<dim3(static_cast<unsigned>(full), ny, nz), kPrefetchWarps * 32, 0, s>>>(
+            c, scales, E, C, log2b, lb, oc, out_scales);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  if (C % Geo4<4>::CTA != 0)
+    k_dequant_reduce_requant<4, KC, true><<<dim3(1, ny, nz), kThreads, 0, s>>>(
+        c, scales, E, C, log2b, KC, lb, static_cast<int>(full), oc, out_scales);
+  return cudaGetLastError();
+}
+
 // INT8, M = KC (1 or 2) sources: the whole 4096-output tiles through the wide kernel, a ragged
 // last tile through the register kernel at that tile offset.
 template <int KC>
@@ -775,11 +853,13 @@ static cudaError_t drr_bits(const void* c, const float* sc, int64_t E, int64_t C
     if (M == 2) return run_wide8<2>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
     return run_wide8<1>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
   } else {
+    // INT4 with one or two sources: two tiles per CTA, both loaded before the first is
+    // converted (2^30 codes, K = 2: 181-189 us against 257-274 us staged)
+    if (M == 2) return run_prefetch<2>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
+    if (M == 1) return run_prefetch<1>(c, sc, E, C, log2b, N, lb, le, oc, os, s);
     switch (chunk_for(M)) {
       case 8: return run_drr<BITS, 8>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-      case 4: return run_drr<BITS, 4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-      case 2: return run_drr<BITS, 2>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
-      default: return run_drr<BITS, 1>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
+      default: return run_drr<BITS, 4>(c, sc, E, C, log2b, N, M, lb, le, oc, os, s);
     }
   }
 }
