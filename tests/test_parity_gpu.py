@@ -195,6 +195,30 @@ def test_sixteen_byte_aligned_buffers_are_served(dtype, bits):
     assert torch.equal(tc, c0) and torch.equal(ts.view(torch.int32), s0.view(torch.int32))
 
 
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("N,M", [(3, 2), (2, 1)])
+def test_sixteen_byte_aligned_small_hops(N, M, bits):
+    """The fused hop with one or two sources on codes that are 16-byte but not 32-byte
+    aligned (INT8: the wide kernel's 128-bit loads and stores; INT4: the kernel that loads
+    two tiles ahead), over whole tiles and a ragged last tile."""
+    B = 256
+    W = N * M
+    E = W * (2 * 8192 + 512)
+    C = E // M
+    g = inputs.draw("laplace", W * E, seed=21 + bits + M, dtype=torch.bfloat16,
+                    device=DEV).reshape(W, E)
+    c0 = at16((W, zb.zpp_code_bytes(E, bits)), torch.uint8)
+    s0 = at16((W, E // B), torch.float32)
+    zpp.qgz_reorder_quant(g, B, bits, N, M, codes=c0, scales=s0)
+    c1 = at16((W, zb.zpp_code_bytes(C, bits)), torch.uint8)
+    s1 = at16((W, C // B), torch.float32)
+    zpp.dequant_reduce_requant(c0, s0, E, B, bits, N, M, out_codes=c1, out_scales=s1)
+    want = oracle.qgz_pipeline(bits16(g), oracle.BF16, B, bits, N, M)
+    for a, b, name in zip((c0, s0, c1, s1), want[:4], ("codes", "scales", "hop-1 codes",
+                                                      "hop-1 scales")):
+        assert np.array_equal(host(a).view(np.uint8), b.view(np.uint8)), name
+
+
 def test_shard_launches_equal_one_launch():
     """qwZ quantises per rank; 16 shard launches at their offsets == one launch."""
     n_shard, R, B = 2048 * 24, 16, 2048
