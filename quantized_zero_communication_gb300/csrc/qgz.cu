@@ -23,8 +23,9 @@
 
 namespace zpp {
 
-// Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements) and 16 elements
-// in K5; a CTA tile is 8 warps x one row (4 warps in the INT4 staged kernel).
+// Lanes own 16 code bytes per source in K4 (32 INT4 / 16 INT8 elements; 32 INT8 codes in
+// the wide kernel) and 16 elements in K5; a CTA tile is 8 warps x one row (4 warps in the
+// INT4 staged, the prefetching and the wide kernels).
 //
 // K4 kernels, chosen per launch by drr_bits / run_drr (all give the same bits):
 //   k_dequant_reduce_requant_ring8<KC>          INT8 codes, M >= 3: the bulk-copy ring below;
@@ -41,8 +42,8 @@ namespace zpp {
 // With chunks of 4 or more sources, kSplitWords of the 4 code words per source go through
 // int4x8_to_f2_eo, which shares the conversion between the integer and fp32 pipes. Measured
 // on GB300 (4 x 8 bucket, K = 8): 3 of 4 words is fastest at both register budgets (3 CTAs
-// per SM for the register-held split kernel, 4 for the staged one); with 2 sources per
-// chunk the plain conversion is faster.
+// per SM for the register-held split kernel, 4 for the staged one). The prefetching kernel
+// (one or two sources, two tiles in flight) measured fastest with all 4 words split.
 constexpr int kSplitWords = 3;
 constexpr int kSplitMinCtas = 3;   // k_dequant_reduce_requant_split: 80 registers
 constexpr int kStagedMinCtas = 4;  // k_dequant_reduce_requant_staged (KC <= 8): 64 registers
