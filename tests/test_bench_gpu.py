@@ -38,6 +38,7 @@ def test_bench_line_has_the_contract_keys():
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     assert e2e["checked"] is True  # host outputs equal the device-only path's, bit for bit
     # the weakest of the target kernels, and the metric's two named parts
+    assert roof["spec_peak"] == 7900.0 and abs(roof["frac_spec"] - roof["achieved"] / 7900.0) < 1e-3
     rmin = d["roofline_min"]
     targets = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant")
     assert rmin["kernel"] in targets
