@@ -242,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, kSplitMinCtas)
                                      out_scales);
 }
 
-// CTA of the staged kernel: 4 warps for INT4 codes (a 4096-code block is 4 rows, so every
-// block fits one CTA), 8 for INT8 (8 rows of 512). Measured on GB300 (4 x 8 bucket, INT4,
-// 8 sources): 65.8 us with CTAs of 1, 2 or 4 warps against 67.6 us with 8.
+// CTA of the staged kernel, which takes INT4 codes only (INT8 codes go to the ring or the
+// wide kernel): 4 warps (a 4096-code block is 4 rows, so every block fits one CTA; an INT8
+// tile would need 8). Measured on GB300 (4 x 8 bucket, 8 sources): 65.8 us with CTAs of 1,
+// 2 or 4 warps against 67.6 us with 8.
 template <int BITS>
 constexpr int staged_warps() { return BITS == 4 ? 4 : 8; }
 template <int BITS, int KC>
@@ -255,8 +256,8 @@ constexpr int staged_min_ctas() {
   return KC > 8 ? 3 * 8 / staged_warps<BITS>() : kStagedMinCtas * 8 / staged_warps<BITS>();
 }
 
-// K4, exactly KC (2, 4, 8 or 16) sources per receiver, full tiles only: every thread
-// stages its 16 code bytes of each source (32 INT4 or 16 INT8 codes) in shared memory with
+// K4, INT4 codes, exactly KC (4, 8 or 16) sources per receiver, full tiles only: every
+// thread stages its 16 code bytes of each source (32 codes) in shared memory with
 // cp.async (the copies do not occupy registers), in two commit groups; the first half of
 // the sources is reduced while the second half is still landing. Each thread reads back only
 // the slots it filled, and every slot is written once per launch, so no barrier is needed.
@@ -268,6 +269,7 @@ __global__ void __launch_bounds__(staged_warps<BITS>() * 32, staged_min_ctas<BIT
                                     const float* __restrict__ scales, int64_t E, int64_t C,
                                     int log2b, int l_begin, uint8_t* __restrict__ out_codes,
                                     float* __restrict__ out_scales) {
+  static_assert(BITS == 4, "INT8 codes take the ring or the wide kernel");
   using G = Geo4<BITS>;
   constexpr int M = KC, H = KC / 2, NT = staged_warps<BITS>() * 32;
   extern __shared__ uint4 stage_mem[];  // [KC][NT], staged_smem_bytes<BITS, KC>()
@@ -719,10 +721,13 @@ static cudaError_t run_staged(const uint8_t* c, const float* scales, int64_t E, 
   return cudaGetLastError();
 }
 
+// INT4 codes, 3 or more sources, in chunks of KC (4 or 8): the staged kernel when one chunk
+// holds every source (M = KC, or M = 16 as one stage of 16), else the split / register kernels.
 template <int BITS, int KC>
 static cudaError_t run_drr(const void* codes, const float* scales, int64_t E, int64_t C, int log2b,
                            int N, int M, int lb, int le, void* out_codes, float* out_scales,
                            cudaStream_t s) {
+  static_assert(BITS == 4 && KC >= 4, "one or two sources and INT8 codes have their own kernels");
   constexpr int CTA = Geo4<BITS>::CTA;
   const uint8_t* c = static_cast<const uint8_t*>(codes);
   uint8_t* oc = static_cast<uint8_t*>(out_codes);
