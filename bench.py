@@ -44,8 +44,9 @@ KERNEL_SOURCES = {"K1_quant": ["quant.cu", "quant_tile.cuh", "zpp_device.cuh"],
                   "K3_reorder_quant": ["reorder_quant.cu", "quant_tile.cuh", "zpp_device.cuh"],
                   "K4_dequant_reduce_requant": ["qgz.cu", "zpp_device.cuh"],
                   "K5_dequant_reduce": ["qgz.cu", "zpp_device.cuh"]}
-# The kernels the spec throughput target names: quantise (K1, and K3 for the
-# gradients), dequantise (K2) and the fused dequant-reduce-requant (K4).
+# The kernels held to the throughput target (80 % of the measured HBM bandwidth at 256M
+# elements and more): quantise (K1, and K3 for the gradients), dequantise (K2) and the fused
+# dequant-reduce-requant (K4).
 TARGET_KERNELS = ("K1_quant", "K2_dequant", "K3_reorder_quant", "K4_dequant_reduce_requant")
 
 
